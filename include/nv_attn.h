@@ -1,0 +1,233 @@
+/*
+ * nv_attn.h — C ABI of libnvattn.so: the device work of one Qwen3 attention
+ * sublayer as nano-vllm runs it, written for NVIDIA GB300 (sm_103a).
+ *
+ * Operations, in the order one layer calls them:
+ *   nv_add_rmsnorm          fused residual add + RMSNorm (input_layernorm)
+ *   nv_qknorm_rope          per-head RMSNorm of q and k, then RoPE, in place
+ *   nv_store_kvcache        scatter new K/V rows into the paged cache
+ *   nv_prefill_attn_varlen  causal GQA attention over packed sequences
+ *   nv_decode_attn_paged    single-query GQA attention over the paged cache
+ * plus nv_rope_cos_sin_cache (builds the RoPE table once) and the decode
+ * workspace query.
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor is a caller-owned DEVICE pointer (allocated e.g. by
+ *     PyTorch).  The library never allocates, frees, synchronises or reads
+ *     results back; every call only enqueues kernels on `stream` (a
+ *     cudaStream_t; NULL means the legacy default stream) and returns.
+ *   - bf16 tensors are passed as `nv_bf16_t` (the 16 raw bits of a bfloat16).
+ *     Integer metadata is int32 (slot_mapping, block_tables, context_lens,
+ *     cu_seqlens) except positions, which are int64, as in nano-vllm.
+ *   - Strides are in ELEMENTS.  Within a token, heads are contiguous and
+ *     head_dim is contiguous (stride 1), matching the views nano-vllm makes
+ *     of its packed qkv buffer.
+ *   - Return value: NV_OK (0) or a negative NV_E* code.  Arguments are
+ *     checked on the host before anything is launched; on any error nothing
+ *     is launched and device memory is untouched.  NV_ELAUNCH reports a
+ *     failed launch (cudaGetLastError after the launch).
+ *   - Device-side index faults that the host cannot see (a slot, block id,
+ *     context length or position out of range) never trap: the element is
+ *     skipped and, if `err_count` is non-NULL, atomically counted there.
+ *   - No entry point waits on another CTA.  Waits inside a CTA (its own
+ *     copy and tensor-core pipeline) give up after about a second, count
+ *     the failure in err_count and let the kernel finish.
+ *   - Calls are asynchronous and allocate nothing.
+ *
+ * Sources are cited by page title and section.
+ */
+#ifndef NV_ATTN_H
+#define NV_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t nv_bf16_t;
+
+#define NV_OK            0
+#define NV_EINVAL       -1  /* null pointer, negative or inconsistent size  */
+#define NV_EUNSUPPORTED -2  /* shape outside what the kernels implement     */
+#define NV_EALIGN       -3  /* pointer or stride not 16-byte aligned        */
+#define NV_EWORKSPACE   -4  /* decode workspace missing or too small        */
+#define NV_ELAUNCH      -5  /* kernel launch failed                          */
+#define NV_EDRIVER      -6  /* TMA descriptor could not be built            */
+
+/* Human-readable name of a status code (static string). */
+const char *nv_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int nv_version(void);
+
+/*
+ * RoPE table.  "3.3 Model skeleton and core operators", sec. 3: cos and sin
+ * of position * inv_freq, inv_freq[i] = 1 / base^(2i / rotary_dim), stored
+ * as one row per position, cos half then sin half.
+ *   cos_sin      [max_position, rotary_dim] fp32, written.
+ *   base         rope_theta (1e6 for Qwen3).
+ * The angle is formed in fp64 on the device and only the result is rounded
+ * to fp32 (the pages form it in fp32; at position 40959 that costs up to
+ * ~2e-3 rad, which this table avoids).  rotary_dim must be even, <= 1024.
+ */
+int nv_rope_cos_sin_cache(float *cos_sin, int max_position, int rotary_dim,
+                          double base, void *stream);
+
+/*
+ * Fused residual add + RMSNorm.  "3.3 Model skeleton and core operators",
+ * sec. 2 (add_rms_forward / rms_forward); "同一个 Qwen3，两种写法", sec. 3.6.
+ * Per row t of H features:
+ *   s = x + residual (fp32);  residual_out = bf16(s);
+ *   out = bf16(s * rsqrt(mean(s^2) + eps) * weight)
+ * residual == NULL gives the plain RMSNorm of x (first layer); residual_out
+ * is then not written and may be NULL.
+ *   x, residual, out, residual_out   [T, H] bf16, contiguous rows.
+ *   weight                           [H] bf16 (gamma).
+ * residual_out may alias residual (in place); out may alias x.  Other
+ * overlaps are undefined.  Requires H % 8 == 0, 8 <= H <= 16384, all
+ * pointers 16-byte aligned.  T == 0 is a no-op.
+ */
+int nv_add_rmsnorm(const nv_bf16_t *x, const nv_bf16_t *residual,
+                   const nv_bf16_t *weight, nv_bf16_t *out,
+                   nv_bf16_t *residual_out, int64_t T, int H, float eps,
+                   void *stream);
+
+/*
+ * QK-Norm + RoPE, in place.  "3.3 Model skeleton and core operators",
+ * sec. 8 (q_norm / k_norm over head_dim when qkv_bias is false, then
+ * rotary_emb) and sec. 3 (half-split rotation: dimension i pairs with
+ * i + head_dim/2); "Nano-vLLM 源码解读 第17篇", sec. 4.
+ * For each token t and head h of q (weight q_norm_weight) and of k
+ * (weight k_norm_weight):
+ *   n = x * rsqrt(mean(x^2) + eps) * w                  (fp32)
+ *   x[i]       <- bf16(n[i] * cos - n[i+64] * sin)
+ *   x[i + 64]  <- bf16(n[i+64] * cos + n[i] * sin)      (i < 64)
+ * with (cos, sin) = cos_sin[positions[t]].  V is never touched.
+ *   q            [T, Hq, head_dim] bf16, token stride q_tok_stride.
+ *   k            [T, Hkv, head_dim] bf16, token stride k_tok_stride.
+ *   cos_sin      [max_position, head_dim] fp32 (nv_rope_cos_sin_cache).
+ *   positions    [T] int64.
+ * A position outside [0, max_position) leaves that token's q and k
+ * unchanged and is counted in err_count.  Requires head_dim == 128,
+ * token strides multiples of 8, pointers 16-byte aligned.
+ */
+int nv_qknorm_rope(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
+                   int64_t k_tok_stride, const nv_bf16_t *q_norm_weight,
+                   const nv_bf16_t *k_norm_weight, const float *cos_sin,
+                   int max_position, const int64_t *positions, int64_t T,
+                   int Hq, int Hkv, int head_dim, float eps, int *err_count,
+                   void *stream);
+
+/*
+ * store_kvcache.  "3.3 Model skeleton and core operators", sec. 7.1;
+ * "Nano-vLLM 源码解读 第17篇", sec. 5.1.  For every token n with
+ * slot_mapping[n] != -1, copy its D = Hkv * head_dim key elements to row
+ * slot_mapping[n] of the cache viewed as [num_slots, D], and likewise the
+ * value.  A bit copy: the cache receives exactly the input bits.
+ *   key, value        [N, Hkv, head_dim] bf16, token strides key_tok_stride,
+ *                     value_tok_stride (heads contiguous).
+ *   k_cache, v_cache  [num_blocks, block_size, Hkv, head_dim] bf16,
+ *                     num_slots = num_blocks * block_size.
+ *   slot_mapping      [N] int32 (-1 = padding, skipped silently).
+ * Any other slot outside [0, num_slots) is skipped and counted.  Requires
+ * D % 8 == 0, D <= 8192, strides multiples of 8, 16-byte aligned pointers.
+ * Two tokens naming the same slot leave one of them there (unspecified
+ * which).
+ */
+int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride,
+                     const nv_bf16_t *value, int64_t value_tok_stride,
+                     nv_bf16_t *k_cache, nv_bf16_t *v_cache,
+                     const int32_t *slot_mapping, int64_t N, int Hkv,
+                     int head_dim, int64_t num_slots, int *err_count,
+                     void *stream);
+
+/*
+ * Varlen causal prefill attention.  "3.3 Model skeleton and core
+ * operators", sec. 7.2 (flash_attn_varlen_func, scale head_dim^-0.5,
+ * causal=True); "同一个 Qwen3，两种写法", sec. 3.2 (packed [T, ...] layout,
+ * cu_seqlens boundaries, block-diagonal causal mask); "nano-vllm code
+ * walkthrough", Prefill stage case 1 (contiguous k/v, q and k lengths equal).
+ * For sequence b (queries [cu_seqlens_q[b], cu_seqlens_q[b+1]), keys
+ * [cu_seqlens_k[b], cu_seqlens_k[b+1])), query head h and query row i:
+ *   o = sum_{j <= i} softmax_j(softmax_scale * <q_i, k_j>) v_j
+ * with k, v taken from kv head h / (Hq / Hkv).  Computed on tcgen05 tensor
+ * cores: bf16 operands, fp32 accumulation in tensor memory, fp32 softmax.
+ *   q      [total_q, Hq, head_dim] bf16, token stride q_tok_stride.
+ *   k, v   [total_k, Hkv, head_dim] bf16, token strides k_/v_tok_stride.
+ *   o      [total_q, Hq, head_dim] bf16, contiguous, written.
+ *   cu_seqlens_q, cu_seqlens_k   [B + 1] int32, device.
+ *   max_seqlen_q, max_seqlen_k   upper bounds of the per-sequence lengths
+ *                                (they size the grid; larger is safe).
+ * This version requires causal == 1 and equal q and k lengths per
+ * sequence (cu_seqlens_q == cu_seqlens_k element-wise; prefill without a
+ * cached prefix).  Rows of other sequences that share a 128-row tile are
+ * read but masked, so every row of k and v must hold finite values.
+ * Requires head_dim == 128, token strides multiples of 8, 16-byte aligned
+ * pointers, total_q, total_k < 2^31.  err_count (optional) counts pipeline
+ * waits that gave up after about a second; only a defect can cause one, and
+ * the affected output rows are then left unwritten.
+ */
+int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
+                           const nv_bf16_t *k, int64_t k_tok_stride,
+                           const nv_bf16_t *v, int64_t v_tok_stride,
+                           nv_bf16_t *o, const int32_t *cu_seqlens_q,
+                           const int32_t *cu_seqlens_k, int B, int64_t total_q,
+                           int64_t total_k, int max_seqlen_q, int max_seqlen_k,
+                           int Hq, int Hkv, int head_dim, float softmax_scale,
+                           int causal, int *err_count, void *stream);
+
+/*
+ * Bytes of fp32 workspace nv_decode_attn_paged needs for these sizes and
+ * this kv_split_tokens (0 = automatic, resolved exactly as the decode call
+ * resolves it on the current device).  Returns 0 when no workspace is
+ * needed and also on invalid sizes.
+ */
+size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim,
+                                     int max_blocks_per_seq, int block_size,
+                                     int kv_split_tokens);
+
+/*
+ * Paged decode attention.  "3.3 Model skeleton and core operators", sec. 7.2
+ * (flash_attn_with_kvcache with cache_seqlens = context_lens and
+ * block_table); "nano-vllm code walkthrough", Decode Stage; split-KV with a
+ * log-sum-exp merge is the rescaling identity of "Nano-vLLM 源码解读 第17篇",
+ * sec. 5.2 applied across key ranges.
+ * For sequence b and query head h, with L = context_lens[b] (it counts the
+ * token just written by nv_store_kvcache):
+ *   o[b, h] = sum_{j < L} softmax_j(softmax_scale * <q[b,h], K_j>) V_j,
+ *   K_j = k_cache[block_tables[b][j / block_size], j % block_size, h / G]
+ * with G = Hq / Hkv (same for V).  L == 0 writes zeros.
+ *   q             [B, Hq, head_dim] bf16, token stride q_tok_stride.
+ *   k_cache, v_cache  [num_blocks, block_size, Hkv, head_dim] bf16.
+ *   block_tables  [B, max_blocks_per_seq] int32 (entries past
+ *                 ceil(L / block_size) are never read; -1 padding is fine).
+ *   context_lens  [B] int32.
+ *   o             [B, Hq, head_dim] bf16, contiguous, written.
+ *   kv_split_tokens  keys per split (rounded up to a multiple of 64);
+ *                 0 = automatic.  A sequence longer than one split is
+ *                 processed by several CTAs whose partial (O, log-sum-exp)
+ *                 go to `workspace` and are merged by a second kernel.
+ *   workspace     device buffer of at least
+ *                 nv_decode_attn_workspace_size(...) bytes (may be NULL
+ *                 when that size is 0); contents on entry are ignored.
+ * A block id outside [0, num_blocks) or L > max_blocks_per_seq *
+ * block_size is counted in err_count; the offending keys are skipped.
+ * Requires head_dim == 128, block_size % 64 == 0, 1 <= G <= 16, 16-byte
+ * aligned pointers, q_tok_stride a multiple of 8, B <= 65535.
+ */
+int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
+                         const nv_bf16_t *k_cache, const nv_bf16_t *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, nv_bf16_t *o, int B,
+                         int Hq, int Hkv, int head_dim, int block_size,
+                         int64_t num_blocks, float softmax_scale,
+                         int kv_split_tokens, void *workspace,
+                         size_t workspace_bytes, int *err_count, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NV_ATTN_H */

@@ -1,0 +1,79 @@
+// Host-side interface between the ABI translation unit (abi.cu, which checks
+// arguments) and the translation units that own each kernel.  Launchers
+// assume their arguments were already validated and return the
+// cudaGetLastError() of their launches.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nvattn {
+
+cudaError_t launch_rope_cos_sin(float *cos_sin, int max_position, int rotary_dim, double base,
+                                cudaStream_t s);
+
+cudaError_t launch_add_rmsnorm(const uint16_t *x, const uint16_t *residual,
+                               const uint16_t *weight, uint16_t *out, uint16_t *residual_out,
+                               int64_t T, int H, float eps, cudaStream_t s);
+
+cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64_t k_stride,
+                               const uint16_t *qw, const uint16_t *kw, const float *cos_sin,
+                               int max_position, const int64_t *positions, int64_t T, int Hq,
+                               int Hkv, float eps, int *err_count, cudaStream_t s);
+
+cudaError_t launch_store_kvcache(const uint16_t *key, int64_t key_stride, const uint16_t *value,
+                                 int64_t value_stride, uint16_t *k_cache, uint16_t *v_cache,
+                                 const int32_t *slot_mapping, int64_t N, int D,
+                                 int64_t num_slots, int *err_count, cudaStream_t s);
+
+// ------------------------------------------------------------------ decode
+struct DecodeParams {
+    const uint16_t *q;
+    int64_t q_stride;
+    const int32_t *block_tables;
+    int max_blocks;
+    const int32_t *context_lens;
+    uint16_t *o;
+    int B, Hq, Hkv, block_size;
+    int64_t num_blocks;
+    float scale_log2;          // softmax_scale * log2(e)
+    int split_tokens;          // keys per split, multiple of 64
+    int max_splits;            // ceil(max_blocks * block_size / split_tokens)
+    float *ws_o;               // [B * Hq * max_splits, 128] partial outputs
+    float *ws_lse;             // [B * Hq * max_splits] log2-sum-exp of each split
+    int *err_count;
+};
+
+// Keys per split for given sizes (kv_split_tokens 0 = automatic).
+int decode_resolve_split(int B, int Hkv, int max_blocks, int block_size, int kv_split_tokens,
+                         int num_sms);
+size_t decode_workspace_bytes(int B, int Hq, int max_splits);
+
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &k_map,
+                          const CUtensorMap &v_map, cudaStream_t s);
+
+// ----------------------------------------------------------------- prefill
+struct PrefillParams {
+    const int32_t *cu_seqlens_q;
+    const int32_t *cu_seqlens_k;
+    uint16_t *o;
+    int B, Hq, Hkv;
+    int max_seqlen_q;
+    float scale_log2;
+    int *err_count;
+};
+
+cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
+                           const CUtensorMap &k_map, const CUtensorMap &v_map,
+                           cudaStream_t s);
+
+// --------------------------------------------------------------------- TMA
+// Build a bf16 tiled tensor map with 128-byte swizzling (the innermost box
+// dimension must be 64 elements).  dims/strides are innermost first; strides
+// are in bytes for dims 1..rank-1.  Returns false on failure.
+bool make_tensor_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                          const uint64_t *strides_bytes, const uint32_t *box);
+
+}  // namespace nvattn
