@@ -30,8 +30,11 @@
  *     context length or position out of range) never trap: the element is
  *     skipped and, if `err_count` is non-NULL, atomically counted there.
  *   - No entry point waits on another CTA.  Waits inside a CTA (its own
- *     copy and tensor-core pipeline) give up after about a second, count
- *     the failure in err_count and let the kernel finish.
+ *     copy and tensor-core pipeline) give up after about a second; the
+ *     kernel then sets bit 30 (NV_ERR_PIPELINE_FAILURE) of err_count, leaves
+ *     the affected outputs unwritten and finishes.  CTAs that start after
+ *     the bit is set skip their work.  Only a defect can cause this; clear
+ *     err_count before reusing it.
  *   - Calls are asynchronous and allocate nothing.
  *
  * Sources are cited by page title and section.
@@ -46,6 +49,12 @@
 extern "C" {
 #endif
 
+#if defined(__GNUC__)
+#define NV_API __attribute__((visibility("default")))
+#else
+#define NV_API
+#endif
+
 typedef uint16_t nv_bf16_t;
 
 #define NV_OK            0
@@ -56,11 +65,14 @@ typedef uint16_t nv_bf16_t;
 #define NV_ELAUNCH      -5  /* kernel launch failed                          */
 #define NV_EDRIVER      -6  /* TMA descriptor could not be built            */
 
+/* Bit of *err_count set when an in-kernel pipeline wait gave up. */
+#define NV_ERR_PIPELINE_FAILURE (1 << 30)
+
 /* Human-readable name of a status code (static string). */
-const char *nv_status_string(int status);
+NV_API const char *nv_status_string(int status);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
-int nv_version(void);
+NV_API int nv_version(void);
 
 /*
  * RoPE table.  "3.3 Model skeleton and core operators", sec. 3: cos and sin
@@ -72,7 +84,7 @@ int nv_version(void);
  * to fp32 (the pages form it in fp32; at position 40959 that costs up to
  * ~2e-3 rad, which this table avoids).  rotary_dim must be even, <= 1024.
  */
-int nv_rope_cos_sin_cache(float *cos_sin, int max_position, int rotary_dim,
+NV_API int nv_rope_cos_sin_cache(float *cos_sin, int max_position, int rotary_dim,
                           double base, void *stream);
 
 /*
@@ -89,7 +101,7 @@ int nv_rope_cos_sin_cache(float *cos_sin, int max_position, int rotary_dim,
  * overlaps are undefined.  Requires H % 8 == 0, 8 <= H <= 16384, all
  * pointers 16-byte aligned.  T == 0 is a no-op.
  */
-int nv_add_rmsnorm(const nv_bf16_t *x, const nv_bf16_t *residual,
+NV_API int nv_add_rmsnorm(const nv_bf16_t *x, const nv_bf16_t *residual,
                    const nv_bf16_t *weight, nv_bf16_t *out,
                    nv_bf16_t *residual_out, int64_t T, int H, float eps,
                    void *stream);
@@ -113,7 +125,7 @@ int nv_add_rmsnorm(const nv_bf16_t *x, const nv_bf16_t *residual,
  * unchanged and is counted in err_count.  Requires head_dim == 128,
  * token strides multiples of 8, pointers 16-byte aligned.
  */
-int nv_qknorm_rope(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
+NV_API int nv_qknorm_rope(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
                    int64_t k_tok_stride, const nv_bf16_t *q_norm_weight,
                    const nv_bf16_t *k_norm_weight, const float *cos_sin,
                    int max_position, const int64_t *positions, int64_t T,
@@ -136,7 +148,7 @@ int nv_qknorm_rope(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
  * Two tokens naming the same slot leave one of them there (unspecified
  * which).
  */
-int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride,
+NV_API int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride,
                      const nv_bf16_t *value, int64_t value_tok_stride,
                      nv_bf16_t *k_cache, nv_bf16_t *v_cache,
                      const int32_t *slot_mapping, int64_t N, int Hkv,
@@ -165,11 +177,10 @@ int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride,
  * cached prefix).  Rows of other sequences that share a 128-row tile are
  * read but masked, so every row of k and v must hold finite values.
  * Requires head_dim == 128, token strides multiples of 8, 16-byte aligned
- * pointers, total_q, total_k < 2^31.  err_count (optional) counts pipeline
- * waits that gave up after about a second; only a defect can cause one, and
- * the affected output rows are then left unwritten.
+ * pointers, total_q, total_k < 2^31.  err_count (optional) only records
+ * NV_ERR_PIPELINE_FAILURE.
  */
-int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
+NV_API int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
                            const nv_bf16_t *k, int64_t k_tok_stride,
                            const nv_bf16_t *v, int64_t v_tok_stride,
                            nv_bf16_t *o, const int32_t *cu_seqlens_q,
@@ -184,7 +195,7 @@ int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
  * resolves it on the current device).  Returns 0 when no workspace is
  * needed and also on invalid sizes.
  */
-size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim,
+NV_API size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim,
                                      int max_blocks_per_seq, int block_size,
                                      int kv_split_tokens);
 
@@ -217,7 +228,7 @@ size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim,
  * Requires head_dim == 128, block_size % 64 == 0, 1 <= G <= 16, 16-byte
  * aligned pointers, q_tok_stride a multiple of 8, B <= 65535.
  */
-int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
+NV_API int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
                          const nv_bf16_t *k_cache, const nv_bf16_t *v_cache,
                          const int32_t *block_tables, int max_blocks_per_seq,
                          const int32_t *context_lens, nv_bf16_t *o, int B,

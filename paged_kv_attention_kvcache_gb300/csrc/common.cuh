@@ -28,6 +28,25 @@ __device__ __forceinline__ void count_error(int *err_count, int n = 1) {
     if (err_count) atomicAdd(err_count, n);
 }
 
+// Bit set in err_count when a pipeline wait gave up.  CTAs that start after
+// it is set skip their work, so a defect costs one timeout, not one per CTA.
+constexpr int kPipelineFailureBit = 1 << 30;
+
+__device__ __forceinline__ void flag_pipeline_failure(int *err_count) {
+    if (err_count) atomicOr(err_count, kPipelineFailureBit);
+}
+
+// CTA-uniform: thread 0 reads the flag and the answer is broadcast, so all
+// threads of the CTA leave together (call it before any other barrier use).
+__device__ __forceinline__ bool pipeline_failed_before(const int *err_count) {
+    __shared__ int failed;
+    if (threadIdx.x == 0)
+        failed = err_count ? (*reinterpret_cast<const volatile int *>(err_count) &
+                              kPipelineFailureBit) : 0;
+    __syncthreads();
+    return failed != 0;
+}
+
 // 2^x on the SFU (PTX ex2.approx; -inf gives +0).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

@@ -72,7 +72,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         return;
     }
     const int t0 = split * p.split_tokens;
-    if (t0 >= L) return;
+    if (t0 >= L) return;                                     // uniform across the CTA
+    if (pipeline_failed_before(p.err_count)) return;
     const int t1 = min(L, t0 + p.split_tokens);
     const int n_tiles = (t1 - t0 + kTile - 1) / kTile;
     const int n_splits = (L + p.split_tokens - 1) / p.split_tokens;
@@ -105,7 +106,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                 const int stage = i % kStages;
                 if (i >= kStages && !mbar_wait(&empty[stage], ((i / kStages) & 1) ^ 1)) {
                     timed_out = 1;
-                    count_error(p.err_count);
+                    flag_pipeline_failure(p.err_count);
                     break;
                 }
                 const int tok = t0 + i * kTile;
@@ -163,7 +164,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         const int stage = i % kStages;
         if (!mbar_wait(&full[stage], (i / kStages) & 1)) {
             ok = false;
-            if (lane == 0) count_error(p.err_count);
+            if (lane == 0) flag_pipeline_failure(p.err_count);
             break;
         }
         const int tok0 = t0 + i * kTile + warp * 16;        // first token of this warp's slice

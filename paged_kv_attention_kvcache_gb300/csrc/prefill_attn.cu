@@ -124,7 +124,7 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void record_failure(Barriers *bars, int *err_count) {
-    if (atomicExch(&bars->failed, 1) == 0) count_error(err_count);
+    if (atomicExch(&bars->failed, 1) == 0) flag_pipeline_failure(err_count);
 }
 
 }  // namespace
@@ -140,6 +140,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     const int k_start = __ldg(p.cu_seqlens_k + b);
     const int q0 = qt * kBM;
     if (q0 >= L) return;                                    // uniform across the CTA
+    if (pipeline_failed_before(p.err_count)) return;
     const int n_kv = qt + 1;                                 // causal: key tiles 0..qt
     const int kvh = h / (p.Hq / p.Hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -1,0 +1,60 @@
+"""Helpers for the GPU parity tests: device transfer of bf16 bit arrays and the
+tolerance check the tests share.
+
+Tolerance (floating-point outputs, bf16): with e_i = |gpu_i - ref_i| /
+max(1, |ref_i|) against the fp64 oracle, max e <= 2e-2 and mean e <= 2e-3.
+For |ref| <= 1 that is the absolute bound as stated; above 1 it grows with
+the value, because rounding the output to bf16 alone already costs up to
+2^-9 |ref| (0.031 at |ref| = 16).
+"""
+import numpy as np
+import torch
+
+import workloads as wl
+
+MAX_TOL = 2e-2
+MEAN_TOL = 2e-3
+
+
+def dev(bits: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bits (numpy) -> bf16 CUDA tensor of the same shape."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 bits (numpy)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def dev_i32(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def dev_i64(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).cuda()
+
+
+def err_counter() -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def check_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str,
+                max_tol: float = MAX_TOL, mean_tol: float = MEAN_TOL) -> dict:
+    g = wl.bf16_bits_to_f32(gpu_bits).astype(np.float64).reshape(ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    absdiff = np.abs(g - ref)
+    e = absdiff / np.maximum(1.0, np.abs(ref))
+    stats = dict(max_err=float(e.max()) if e.size else 0.0,
+                 mean_err=float(e.mean()) if e.size else 0.0,
+                 max_abs=float(absdiff.max()) if e.size else 0.0)
+    assert stats["max_err"] <= max_tol, f"{what}: max err {stats}"
+    assert stats["mean_err"] <= mean_tol, f"{what}: mean err {stats}"
+    return stats
+
+
+def rope_table(max_position: int = wl.MAX_POSITION, base: float = wl.ROPE_BASE) -> torch.Tensor:
+    import paged_kv_attention_kvcache_gb300 as nv
+    t = torch.empty(max_position, 128, dtype=torch.float32, device="cuda")
+    nv.nv_rope_cos_sin_cache(t, base)
+    return t

@@ -1,0 +1,145 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; bad arguments are rejected on the host with the documented codes
+before anything is launched (so these run without a GPU).  Faults are made on
+the host only: null pointers, unsupported shapes, misalignment, a workspace
+that is too small."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nv_attn.h")
+NV_OK, NV_EINVAL, NV_EUNSUPPORTED, NV_EALIGN, NV_EWORKSPACE = 0, -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_kvcache_gb300 import build as b
+    b.build()
+    import paged_kv_attention_kvcache_gb300 as nv
+    return nv.library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_ops():
+    names = declared_functions()
+    for op in ("nv_add_rmsnorm", "nv_qknorm_rope", "nv_store_kvcache", "nv_prefill_attn_varlen",
+               "nv_decode_attn_paged"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import paged_kv_attention_kvcache_gb300 as nv
+    names = declared_functions()
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) <= set(nv.ABI_FUNCTIONS) | set(names)
+    assert set(nv.ABI_FUNCTIONS) <= set(names)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.nv_status_string(0) == b"NV_OK"
+    for code in (NV_EINVAL, NV_EUNSUPPORTED, NV_EALIGN, NV_EWORKSPACE, -5, -6):
+        assert lib.nv_status_string(code).startswith(b"NV_E")
+    assert lib.nv_version() >= 100
+
+
+FAKE = 0x10000          # a 16-byte-aligned non-null address; never dereferenced
+MIS = 0x10002           # misaligned
+
+
+def test_add_rmsnorm_rejects_bad_arguments(lib):
+    f = lib.nv_add_rmsnorm
+    assert f(None, None, FAKE, FAKE, None, 4, 1024, 1e-6, None) == NV_EINVAL
+    assert f(FAKE, None, FAKE, FAKE, None, -1, 1024, 1e-6, None) == NV_EINVAL
+    assert f(FAKE, None, FAKE, FAKE, None, 4, 1020, 1e-6, None) == NV_EUNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 4, 1024, 1e-6, None) == NV_EINVAL   # residual_out missing
+    assert f(MIS, None, FAKE, FAKE, None, 4, 1024, 1e-6, None) == NV_EALIGN
+    assert f(FAKE, None, FAKE, FAKE, None, 0, 1024, 1e-6, None) == NV_OK      # empty: no-op
+    assert f(FAKE, None, FAKE, FAKE, None, 4, 1024, float("nan"), None) == NV_EINVAL
+
+
+def test_qknorm_rope_rejects_bad_arguments(lib):
+    f = lib.nv_qknorm_rope
+    ok = dict(q=FAKE, qs=6144, k=FAKE, ks=6144, qw=FAKE, kw=FAKE, cs=FAKE, mp=40960, pos=FAKE,
+              T=4, Hq=32, Hkv=8, d=128, eps=1e-6)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q"], a["qs"], a["k"], a["ks"], a["qw"], a["kw"], a["cs"], a["mp"], a["pos"],
+                 a["T"], a["Hq"], a["Hkv"], a["d"], a["eps"], None, None)
+
+    assert call(d=64) == NV_EUNSUPPORTED
+    assert call(pos=None) == NV_EINVAL
+    assert call(qs=100) == NV_EINVAL                 # stride shorter than Hq * d
+    assert call(qs=4100) == NV_EALIGN                # stride not a multiple of 8
+    assert call(k=MIS) == NV_EALIGN
+    assert call(mp=0) == NV_EINVAL
+    assert call(T=0) == NV_OK
+
+
+def test_store_kvcache_rejects_bad_arguments(lib):
+    f = lib.nv_store_kvcache
+    assert f(FAKE, 1024, FAKE, 1024, FAKE, FAKE, None, 4, 8, 128, 100, None, None) == NV_EINVAL
+    assert f(FAKE, 1024, FAKE, 1024, FAKE, FAKE, FAKE, 4, 1, 6, 100, None, None) == NV_EUNSUPPORTED
+    assert f(FAKE, 1000, FAKE, 1024, FAKE, FAKE, FAKE, 4, 8, 128, 100, None, None) == NV_EINVAL
+    assert f(FAKE, 1032, FAKE, 1028, FAKE, FAKE, FAKE, 4, 8, 128, 100, None, None) == NV_EALIGN
+    assert f(FAKE, 1024, FAKE, 1024, MIS, FAKE, FAKE, 4, 8, 128, 100, None, None) == NV_EALIGN
+    assert f(FAKE, 1024, FAKE, 1024, FAKE, FAKE, FAKE, 0, 8, 128, 100, None, None) == NV_OK
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    f = lib.nv_prefill_attn_varlen
+
+    def call(Hq=32, Hkv=8, d=128, causal=1, q=FAKE, qs=6144, B=2, scale=0.088):
+        return f(q, qs, FAKE, 6144, FAKE, 6144, FAKE, FAKE, FAKE, B, 100, 100, 64, 64, Hq, Hkv, d,
+                 scale, causal, None, None)
+
+    assert call(Hq=30) == NV_EINVAL                  # Hq % Hkv != 0
+    assert call(d=64) == NV_EUNSUPPORTED
+    assert call(causal=0) == NV_EUNSUPPORTED
+    assert call(q=None) == NV_EINVAL
+    assert call(q=MIS) == NV_EALIGN
+    assert call(qs=6148) == NV_EALIGN
+    assert call(scale=0.0) == NV_EINVAL
+    assert call(B=0) == NV_OK
+
+
+def test_decode_rejects_bad_arguments_and_small_workspace(lib):
+    f = lib.nv_decode_attn_paged
+
+    def call(Hq=32, Hkv=8, d=128, bs=256, mb=32, ws=None, wsb=0, q=FAKE, B=4, split=0):
+        return f(q, 4096, FAKE, FAKE, FAKE, mb, FAKE, FAKE, B, Hq, Hkv, d, bs, 1000, 0.088, split,
+                 ws, wsb, None, None)
+
+    assert call(Hq=12) == NV_EINVAL                  # Hq % Hkv != 0
+    assert call(Hq=256, Hkv=8) == NV_EUNSUPPORTED    # group of 32 > 16
+    assert call(d=96) == NV_EUNSUPPORTED
+    assert call(bs=100) == NV_EUNSUPPORTED
+    assert call(q=None) == NV_EINVAL
+    assert call(q=MIS) == NV_EALIGN
+    # A context of 32 blocks with 256-token splits needs a workspace.
+    need = lib.nv_decode_attn_workspace_size(4, 32, 8, 128, 32, 256, 256)
+    assert need == 4 * 32 * 32 * 129 * 4
+    assert call(split=256) == NV_EWORKSPACE
+    assert call(split=256, ws=FAKE, wsb=need - 4) == NV_EWORKSPACE
+    assert call(split=256, ws=MIS, wsb=need) == NV_EALIGN
+    # One split per sequence needs none.
+    assert lib.nv_decode_attn_workspace_size(4, 32, 8, 128, 4, 256, 1024) == 0
+    assert call(B=0) == NV_OK
+
+
+def test_rope_table_rejects_bad_arguments(lib):
+    f = lib.nv_rope_cos_sin_cache
+    assert f(FAKE, 16, 127, 1e6, None) == NV_EINVAL
+    assert f(FAKE, 16, 128, 0.5, None) == NV_EINVAL
+    assert f(None, 16, 128, 1e6, None) == NV_EINVAL
+    assert f(None, 0, 128, 1e6, None) == NV_OK
