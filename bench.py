@@ -74,33 +74,54 @@ def prefill_flops(lengths) -> float:
 
 # ------------------------------------------------------------- clock probe
 class ClockSampler:
+    """nvidia-smi sampled every 100 ms in a reader thread; `window()` keeps
+    the samples taken between mark_start() and mark_end()."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
+        import threading
+        self.samples = []
+        self.t0 = self.t1 = None
         self.proc = None
-        self.gpu = gpu_index
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
-            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        deadline = time.time() + 10
+        while not self.samples and time.time() < deadline:
+            time.sleep(0.02)
 
-    def stop(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def window(self):
         if self.proc is None:
             return None
+        time.sleep(0.25)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        inside = [l for t, l in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
+        used = inside if inside else [l for _, l in self.samples[-3:]]
         sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in used:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -109,13 +130,13 @@ class ClockSampler:
                 smax = float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(self.NAMES, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "in_window": bool(inside)}
 
 
 # ---------------------------------------------------------------- our arm
@@ -214,6 +235,7 @@ def run_ours(args, rank, world, local_rank):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
+    clocks = ClockSampler(local_rank)
     for _ in range(args.warmup):
         decode_layer()
         prefill_layer()
@@ -225,7 +247,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
+    clocks.mark_start()
     t_wall = time.time()
     for _ in range(args.steps):
         flush.zero_()
@@ -237,9 +259,10 @@ def run_ours(args, rank, world, local_rank):
         records.append(e)
     torch.cuda.synchronize()
     wall = time.time() - t_wall
+    clocks.mark_end()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.window()
     dec_ms = [e[0].elapsed_time(e[3]) for e in records]
     attn_ms = [e[1].elapsed_time(e[2]) for e in records]
     pre_ms = [e[3].elapsed_time(e[5]) for e in records]
@@ -309,53 +332,58 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------ oracle side
-def oracle_decode_sample(step: wl.DecodeStep, n_seqs: int):
-    """Time the oracle on the decode step restricted to n_seqs sequences (all
-    heads): add-RMSNorm, QK-Norm + RoPE, and paged decode.  Returns
-    (seconds, algorithmic bytes of that sample, threads)."""
+def oracle_decode_step(step: wl.DecodeStep):
+    """The fp64 oracle on the whole decode step: add-RMSNorm, QK-Norm + RoPE
+    of q and k, and paged decode of every (sequence, head).  Returns
+    (seconds, threads)."""
     import oracle
     s = step.shape
-    sub = np.arange(n_seqs)
+    B = step.context_lens.size
     Q, D = s.q_size, s.kv_size
     t0 = time.time()
-    oracle.add_rmsnorm(step.x[sub], step.residual[sub], step.gamma, wl.RMS_EPS)
-    qb = step.qkv[sub, :Q].reshape(n_seqs, s.hq, 128)
-    kb = step.qkv[sub, Q:Q + D].reshape(n_seqs, s.hkv, 128)
-    q_rot = oracle.round_to_bf16(oracle.qknorm_rope(qb, step.q_norm_w, step.positions[sub]))
-    oracle.qknorm_rope(kb, step.k_norm_w, step.positions[sub])
-    oracle.paged_decode(q_rot, step.pool.k, step.pool.v, step.block_tables[sub],
-                        step.context_lens[sub], SCALE)
-    dt = time.time() - t0
-    sub_step = wl.DecodeStep(shape=s, context_lens=step.context_lens[sub],
-                             positions=step.positions[sub], block_tables=step.block_tables[sub],
-                             slot_mapping=step.slot_mapping[sub], pool=step.pool,
-                             qkv=step.qkv[sub], x=step.x[sub], residual=step.residual[sub],
-                             with_norms=True)
-    return dt, decode_step_bytes(sub_step)["total"], oracle.num_threads()
+    oracle.add_rmsnorm(step.x, step.residual, step.gamma, wl.RMS_EPS)
+    qb = step.qkv[:, :Q].reshape(B, s.hq, 128)
+    kb = step.qkv[:, Q:Q + D].reshape(B, s.hkv, 128)
+    q_rot = oracle.round_to_bf16(oracle.qknorm_rope(qb, step.q_norm_w, step.positions))
+    oracle.qknorm_rope(kb, step.k_norm_w, step.positions)
+    oracle.paged_decode(q_rot, step.pool.k, step.pool.v, step.block_tables, step.context_lens,
+                        SCALE)
+    return time.time() - t0, oracle.num_threads()
+
+
+def oracle_baseline(step: wl.DecodeStep, min_seconds: float = 10.0):
+    """Repeat the oracle's decode step until at least min_seconds of work."""
+    nbytes = decode_step_bytes(step)["total"]
+    times, threads = [], 1
+    while not times or sum(times) < min_seconds:
+        dt, threads = oracle_decode_step(step)
+        times.append(dt)
+    return nbytes * len(times) / sum(times) / 1e9, threads, len(times), sum(times)
 
 
 def run_reference(args):
-    """The CPU reference arm: the fp64 oracle, as it stands, on a bounded
-    sample of the same decode-step workload per step."""
+    """The CPU reference arm: the fp64 oracle, as it stands, on the same
+    decode-step workload, one oracle pass per step."""
     import oracle
     oracle.build()
     step = wl.config3()
-    n = args.ref_seqs
     for _ in range(min(args.warmup, 1)):
-        oracle_decode_sample(step, n)
-    times, nbytes, threads = [], 0, 1
+        oracle_decode_step(step)
+    times, threads = [], 1
     for _ in range(args.steps):
-        dt, nbytes, threads = oracle_decode_sample(step, n)
+        dt, threads = oracle_decode_step(step)
         times.append(dt)
+    nbytes = decode_step_bytes(step)["total"]
     value = nbytes * len(times) / sum(times) / 1e9
-    sample = f"decode step of {n} of 256 sequences (all 32 heads), add-RMSNorm + QK-Norm/RoPE"
+    sample = ("whole qwen3-8b decode step (256 sequences, 32 heads, ctx~U[1024,8192]): "
+              "add-RMSNorm, QK-Norm+RoPE, paged decode; one pass per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "qwen3-8b decode layer step (sampled), fp64 CPU oracle",
-                   "global_batch": n, "seq_len": "ctx~U[1024,8192]", "parallelism": "none"},
+        "config": {"workload": "qwen3-8b decode layer step, fp64 CPU oracle",
+                   "global_batch": 256, "seq_len": "ctx~U[1024,8192]", "parallelism": "none"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -363,15 +391,65 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_ncu_case(which: str, launches: int = 3):
+    """A small case of one kernel for detailed ncu captures: a few GB on the
+    device at most, inputs above L2 size, `launches` calls of the op."""
+    import torch
+    import __graft_entry__
+    import paged_kv_attention_kvcache_gb300 as nv
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).cuda()
+
+    if which == "decode":
+        # Qwen3-8B heads, 64 sequences of 4096 keys: 1.07 GB of K/V.
+        ctx = np.full(64, 4096, np.int32)
+        step = wl.make_decode(9, wl.QWEN3_8B, ctx, 64 * 16 + 8, with_norms=False,
+                              name="ncu.decode")
+        s = step.shape
+        q = dev(step.qkv[:, :s.q_size]).view(64, s.hq, 128)
+        kc, vc = dev(step.pool.k), dev(step.pool.v)
+        bt = torch.from_numpy(step.block_tables).cuda()
+        cl = torch.from_numpy(step.context_lens).cuda()
+        o = torch.empty(64, s.hq, 128, dtype=torch.bfloat16, device="cuda")
+        ws_b = nv.nv_decode_attn_workspace_size(64, s.hq, s.hkv, 128, bt.shape[1], 256, 0)
+        ws = torch.empty(max(1, ws_b // 4), dtype=torch.float32, device="cuda")
+        for _ in range(launches):
+            nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws)
+    else:
+        # Qwen3-8B heads, 8 sequences of 2048 tokens (0.2 GB of q/k/v).
+        lengths = np.full(8, 2048, np.int64)
+        pre = wl.make_prefill(9, wl.QWEN3_8B, lengths, name="ncu.prefill")
+        s = pre.shape
+        T = int(lengths.sum())
+        qkv = dev(pre.qkv)
+        Q, D = s.q_size, s.kv_size
+        q, k, v = (qkv[:, :Q].view(T, s.hq, 128), qkv[:, Q:Q + D].view(T, s.hkv, 128),
+                   qkv[:, Q + D:].view(T, s.hkv, 128))
+        cu = torch.from_numpy(pre.cu_seqlens).cuda()
+        o = torch.empty(T, s.hq, 128, dtype=torch.bfloat16, device="cuda")
+        for _ in range(launches):
+            nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, 2048, 2048, SCALE)
+    torch.cuda.synchronize()
+    print(f"ncu case {which}: {launches} launches done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None,
+                    help="run a small case of one kernel (for ncu captures) and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -394,10 +472,10 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        dt, nb, threads = oracle_decode_sample(r["step"], args.ref_seqs)
-        cpu = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"decode step of {args.ref_seqs} of 256 sequences (all heads): "
-                         f"add-RMSNorm, QK-Norm+RoPE, paged decode; {dt:.1f} s"}
+        val, threads, reps, secs = oracle_baseline(r["step"])
+        cpu = {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"whole decode step (256 seqs x 32 heads: add-RMSNorm, QK-Norm+RoPE, "
+                         f"paged decode) repeated {reps}x, {secs:.1f} s of CPU time"}
     if rank == 0:
         nbytes = r["nbytes"]
         line = {

@@ -75,12 +75,20 @@ def test_decode_forced_splits_match_oracle(split):
 
 
 def test_decode_split_count_invariance():
+    # Splitting only regroups the sum; what changes is where P is rounded to
+    # bf16 (against each split's own running max), which moves outputs by a
+    # few 1e-4 at most.  Every split count must also match the oracle.
     ctx = [3000, 1500, 700, 257]
     q, k, v, bt, ctx = random_case(301, len(ctx), 32, 8, ctx)
-    outs = [wl.bf16_bits_to_f32(run_decode(q, k, v, bt, ctx, split=s)[0]) for s in (64, 320, 0, 4096)]
+    ref = oracle.paged_decode(q, k, v, bt, ctx, SCALE)
+    outs = []
+    for split in (64, 320, 0, 4096):
+        got, err = run_decode(q, k, v, bt, ctx, split=split)
+        assert err == 0
+        check_close(got, ref, f"split={split}")
+        outs.append(wl.bf16_bits_to_f32(got).astype(np.float64))
     for o in outs[1:]:
-        # identical math up to fp32 summation order: within 2 bf16 ulps
-        assert np.max(np.abs(o - outs[0]) / np.maximum(np.abs(outs[0]), 1e-3)) <= 2 ** -7
+        assert np.max(np.abs(o - outs[0])) <= 2e-3
 
 
 def test_decode_empty_context_and_token_stride():
@@ -114,7 +122,7 @@ def test_decode_bad_block_id_is_counted_not_faulted():
     got, err = run_decode(q, k, v, bt, ctx)
     assert err >= 1
     # sequence 1 is unaffected
-    ref = oracle.paged_decode(q, k, v, bt[1:], ctx[1:], SCALE)
+    ref = oracle.paged_decode(q[1:], k, v, bt[1:], ctx[1:], SCALE)
     check_close(got[1:], ref, "decode unaffected sequence")
 
 
