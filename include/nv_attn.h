@@ -237,6 +237,44 @@ NV_API int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
                          int kv_split_tokens, void *workspace,
                          size_t workspace_bytes, int *err_count, void *stream);
 
+/*
+ * Paged decode attention that allocates nothing and takes no workspace.
+ * The paper has no counterpart: it exists for callers that are handed only
+ * their input and output buffers and cannot allocate device memory -- a
+ * plugin inside a host framework that owns every allocation, or a serving
+ * loop that has committed all free HBM to its KV cache and may not call
+ * cudaMalloc while serving.
+ *
+ * Arguments and results are those of nv_decode_attn_paged without
+ * `workspace` / `workspace_bytes`.  The split-KV partial results go to one
+ * library-owned device array of NV_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB),
+ * which every GPU that loads the library holds until the process exits.
+ *   - Returns NV_EWORKSPACE, launching nothing, when these sizes would need
+ *     more than that (nv_decode_attn_workspace_size(...) with the same
+ *     arguments tells in advance); use nv_decode_attn_paged, a larger
+ *     kv_split_tokens, or fewer sequences per call.
+ *   - The first call on each device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose kernels overlap
+ *     on the GPU -- on different streams, or from different threads --
+ *     race on it; serialise them.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define NV_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+NV_API int nv_decode_attn_paged_noalloc(const nv_bf16_t *q, int64_t q_tok_stride,
+                                        const nv_bf16_t *k_cache,
+                                        const nv_bf16_t *v_cache,
+                                        const int32_t *block_tables,
+                                        int max_blocks_per_seq,
+                                        const int32_t *context_lens, nv_bf16_t *o,
+                                        int B, int Hq, int Hkv, int head_dim,
+                                        int block_size, int64_t num_blocks,
+                                        float softmax_scale, int kv_split_tokens,
+                                        int *err_count, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

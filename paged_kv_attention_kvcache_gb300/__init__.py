@@ -33,7 +33,7 @@ __all__ = [
 ABI_FUNCTIONS = (
     "nv_status_string", "nv_version", "nv_rope_cos_sin_cache", "nv_add_rmsnorm",
     "nv_qknorm_rope", "nv_store_kvcache", "nv_prefill_attn_varlen",
-    "nv_decode_attn_workspace_size", "nv_decode_attn_paged",
+    "nv_decode_attn_workspace_size", "nv_decode_attn_paged", "nv_decode_attn_paged_noalloc",
 )
 
 _P, _I64, _I32, _F32, _F64, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -51,6 +51,8 @@ _SIGNATURES = {
     "nv_decode_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "nv_decode_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32,
                               _I64, _F32, _I32, _P, _SZ, _P, _P], _I32),
+    "nv_decode_attn_paged_noalloc": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                      _I32, _I64, _F32, _I32, _P, _P], _I32),
 }
 
 _lock = threading.Lock()
