@@ -41,6 +41,20 @@ METRIC = "paged-attn decode HBM GB/s (% peak); prefill attn TFLOP/s, Qwen3-8B sh
 SCALE = 128 ** -0.5
 
 
+# DRAM bytes per algorithmic byte of the decode attention kernels, from the
+# ncu capture in profiles/decode_attn_qwen3_8b_64x4096.md (reads + writes of
+# decode_split_kernel over its algorithmic bytes), valid only for the kernel
+# source it was taken on.
+DECODE_TRAFFIC = {"ratio": 1.0062, "source_sha256_16": "88592f0223f86772"}
+
+
+def kernel_source_hash(name: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, "paged_kv_attention_kvcache_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -478,6 +492,9 @@ def main():
                          f"paged decode) repeated {reps}x, {secs:.1f} s of CPU time"}
     if rank == 0:
         nbytes = r["nbytes"]
+        traffic = None
+        if kernel_source_hash("decode_attn.cu") == DECODE_TRAFFIC["source_sha256_16"]:
+            traffic = DECODE_TRAFFIC["ratio"] * nbytes["attn"]
         line = {
             "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
@@ -494,7 +511,7 @@ def main():
                 "decode_ms": r["dec_ms"], "prefill_ms": r["pre_ms"]},
             "roofline": {"bound": "hbm", "kernel": "nv_decode_attn_paged (split + merge)",
                          "achieved": r["attn_gbs"], "peak": r["hbm"], "unit": "GB/s",
-                         "frac": r["attn_gbs"] / r["hbm"], "traffic": None,
+                         "frac": r["attn_gbs"] / r["hbm"], "traffic": traffic,
                          "peak_source": r["peak_src"], "launch_ms": r["attn_ms"]},
             "prefill": {"metric": "prefill attn TFLOP/s (causal pairs)", "value": r["ptflops"],
                         "unit": "TFLOP/s", "launch_ms": r["pattn_ms"],
