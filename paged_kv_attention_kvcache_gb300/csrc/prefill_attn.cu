@@ -8,23 +8,30 @@
 // inside each; keys of other sequences are never admitted.
 //
 // How (GB300):
-//  - One CTA per (128-row query tile, query head, sequence).  The grid's z
-//    index runs over query tiles from the last (most keys under the causal
-//    mask) to the first, so the heaviest CTAs are dispatched first.
-//  - Warp 4 issues TMA loads: the Q tile once, then 128-token K and V tiles
-//    into two-deep rings (K and V have separate barriers so QK^T can start
+//  - One CTA per (pair of adjacent 128-row query tiles, query head,
+//    sequence), so every K/V tile loaded serves 256 query rows.  The grid's
+//    z index runs over pairs from the last (most keys under the causal mask)
+//    to the first, so the heaviest CTAs are dispatched first.
+//  - Warp 8 issues TMA loads: both Q tiles once, then 128-token K and V
+//    tiles into two-deep rings (separate K and V barriers, so QK^T can start
 //    before V lands).  Every tile is stored as two 128-byte-swizzled halves
 //    of head_dim, the canonical layout tcgen05 reads.
-//  - Warp 5 allocates tensor memory (512 columns: two S buffers and O) and one
-//    of its threads issues tcgen05.mma: S_j = Q K_j^T (M=N=128, K=128, bf16
-//    in, fp32 accumulate in TMEM), then O += P_{j-1} V_{j-1} with P from
-//    shared memory (K-major) and V read MN-major.  S_{j+1} overlaps the
-//    softmax of S_j.
-//  - Warps 0-3 own one query row per thread (TMEM lane = row): tcgen05.ld of
-//    the S row, causal mask on the diagonal tile, online softmax in base 2
-//    with a lazy rescale (O in TMEM is rescaled only when the running max
-//    grows by more than 2^8, so the stale max bounds p by 256), P written as
-//    bf16 into swizzled shared memory, and finally O / l to global memory.
+//  - Warp 9 allocates all 512 TMEM columns (S_a at 128a, O_a at 256 + 128a
+//    for query tile a) and one of its threads issues tcgen05.mma:
+//    S_a,j = Q_a K_j^T (M = N = 128, bf16 in, fp32 accumulate in TMEM), then
+//    O_a += P_a,j V_j with P read from tensor memory and V MN-major from
+//    shared memory.  The order PV_0,j, S_0,j+1, PV_1,j, S_1,j+1 lets one
+//    softmax warpgroup work while the tensor core serves the other.
+//  - Warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1:
+//    one row per thread (TMEM lane = row).  tcgen05.ld of the S row, causal
+//    mask on the diagonal tile, online softmax in base 2 with a lazy rescale
+//    (O_a in TMEM is rescaled only when the row max grows by more than 2^8,
+//    so the stale max bounds p by 256), and P written back as packed bf16
+//    over the first 64 columns of S_a, where the PV MMA reads it.  The commit
+//    that signals S_a,j also covers PV_a,j-1 (issued before it), so a rescale
+//    of O_a after S_a,j has landed never races the tensor core.
+//  - Epilogue: O_a / l straight to global memory with predicated 16-byte
+//    stores (a TMA store cannot clip at sequence boundaries).
 #include <math.h>
 
 #include "common.cuh"
@@ -34,27 +41,29 @@ namespace nvattn {
 
 namespace {
 
-constexpr int kBM = 128;                        // query rows per CTA
+constexpr int kBM = 128;                        // query rows per tile
 constexpr int kBN = 128;                        // keys per KV tile
+constexpr int kQTiles = 2;                      // query tiles per CTA
 constexpr int kHalf = 128 * 128;                // 128 rows x 64 dims x 2 B = 16 KB
-constexpr int kTileBytes = 2 * kHalf;           // one Q / K / V / P tile, 32 KB
+constexpr int kTileBytes = 2 * kHalf;           // one Q / K / V tile, 32 KB
 constexpr int kKVStages = 2;
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
 constexpr int kOffV = kOffK + kKVStages * kTileBytes;
-constexpr int kOffP = kOffV + kKVStages * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
-constexpr int kPrefillThreads = 192;            // 4 softmax warps, TMA warp, MMA warp
+constexpr int kOffBar = kOffV + kKVStages * kTileBytes;
+constexpr int kSoftmaxWarps = 4 * kQTiles;
+constexpr int kTmaWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kPrefillThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColS = 0, kColO = 256;      // S_a at kColS + 128a, O_a at kColO + 128a
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
 
 struct Barriers {
     uint64_t q_full;
     uint64_t k_full[kKVStages], v_full[kKVStages];
     uint64_t k_empty[kKVStages], v_empty[kKVStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done;
+    uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles];
     uint32_t tmem_base;
     int failed;
 };
@@ -89,6 +98,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// Same with A (M x K, K-major, packed bf16 pairs per 32-bit column) read
+// from tensor memory at column address a_tmem.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(bar)) : "memory");
@@ -120,6 +139,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
           "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -134,14 +162,19 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const PrefillParams p) {
     const int h = blockIdx.x, b = blockIdx.y;
-    const int qt = (int)gridDim.z - 1 - (int)blockIdx.z;   // heaviest tiles first
+    const int pair = (int)gridDim.z - 1 - (int)blockIdx.z;  // heaviest pairs first
     const int q_start = __ldg(p.cu_seqlens_q + b);
     const int L = __ldg(p.cu_seqlens_q + b + 1) - q_start;
     const int k_start = __ldg(p.cu_seqlens_k + b);
-    const int q0 = qt * kBM;
+    const int q0 = pair * kQTiles * kBM;
     if (q0 >= L) return;                                    // uniform across the CTA
     if (pipeline_failed_before(p.err_count)) return;
-    const int n_kv = qt + 1;                                 // causal: key tiles 0..qt
+    // Query tile a holds rows [q0 + 128a, q0 + 128a + 128) and, by causality,
+    // needs key tiles 0 .. qt0 + a; tile 1 may hold no row of this sequence.
+    const int qt0 = pair * kQTiles;
+    const bool has1 = q0 + kBM < L;
+    const int last_tile[2] = {qt0, has1 ? qt0 + 1 : -1};
+    const int n_kv = has1 ? qt0 + 2 : qt0 + 1;
     const int kvh = h / (p.Hq / p.Hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -158,16 +191,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&bars->k_empty[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->s_free[s], 4);
+        for (int a = 0; a < kQTiles; ++a) {
+            mbar_init(&bars->s_full[a], 1);
+            mbar_init(&bars->p_full[a], 4);
+            mbar_init(&bars->o_full[a], 1);
         }
-        mbar_init(&bars->p_full, 4);
-        mbar_init(&bars->pv_done, 1);
         bars->failed = 0;
         fence_mbarrier_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(&bars->tmem_base)), "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -177,18 +209,19 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    uint8_t *sQ = smem + kOffQ;
-    uint8_t *sP = smem + kOffP;
-
-    if (warp == 4) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------------- TMA
         if (lane == 0) {
             tma_prefetch_desc(&q_map);
             tma_prefetch_desc(&k_map);
             tma_prefetch_desc(&v_map);
-            mbar_arrive_expect_tx(&bars->q_full, kTileBytes);
-            tma_load_3d(sQ, &q_map, &bars->q_full, 0, h, q_start + q0);
-            tma_load_3d(sQ + kHalf, &q_map, &bars->q_full, 64, h, q_start + q0);
+            mbar_arrive_expect_tx(&bars->q_full, has1 ? 2 * kTileBytes : kTileBytes);
+            for (int a = 0; a < (has1 ? 2 : 1); ++a) {
+                uint8_t *sQ = smem + kOffQ + a * kTileBytes;
+                const int row = q_start + q0 + a * kBM;
+                tma_load_3d(sQ, &q_map, &bars->q_full, 0, h, row);
+                tma_load_3d(sQ + kHalf, &q_map, &bars->q_full, 64, h, row);
+            }
             for (int j = 0; j < n_kv; ++j) {
                 const int st = j & 1;
                 const uint32_t par = ((j >> 1) - 1) & 1;
@@ -211,93 +244,117 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 tma_load_3d(sV + kHalf, &v_map, &bars->v_full[st], 64, kvh, row);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
             constexpr uint32_t kIdescPV = idesc_bf16(kBM, 128, true);
-            const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
             bool ok = mbar_wait(&bars->q_full, 0);
-            for (int j = 0; ok && j <= n_kv; ++j) {
-                if (j < n_kv) {
-                    const int st = j & 1, sb = j & 1;
-                    if (!mbar_wait(&bars->k_full[st], (j >> 1) & 1) ||
-                        (j >= 2 && !mbar_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t k_addr = smem_u32(smem + kOffK + st * kTileBytes);
-                    const uint32_t d = tmem + (sb ? kColS1 : kColS0);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc_mma(d, smem_desc_sw128(q_addr + off, 16, 1024),
-                               smem_desc_sw128(k_addr + off, 16, 1024), kIdescQK, kk > 0);
-                    }
-                    tc_commit(&bars->s_full[sb]);
-                    tc_commit(&bars->k_empty[st]);
+            int k_ready = -1, v_ready = -1;
+            auto ensure_k = [&](int j) {
+                if (ok && k_ready < j) {
+                    ok = mbar_wait(&bars->k_full[j & 1], (j >> 1) & 1);
+                    k_ready = j;
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, st = jj & 1;
-                    if (!mbar_wait(&bars->p_full, jj & 1) ||
-                        !mbar_wait(&bars->v_full[st], (jj >> 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t v_addr = smem_u32(smem + kOffV + st * kTileBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        // P: K-major like Q.  V: MN-major; 16 keys = 2 swizzle atoms
-                        // (2048 B) per step, the second 64 dims 16 KB (LBO) away.
-                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc_mma(tmem + kColO, smem_desc_sw128(p_addr + poff, 16, 1024),
-                               smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), kIdescPV,
-                               (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&bars->pv_done);
-                    tc_commit(&bars->v_empty[st]);
+            };
+            auto ensure_v = [&](int j) {
+                if (ok && v_ready < j) {
+                    ok = mbar_wait(&bars->v_full[j & 1], (j >> 1) & 1);
+                    v_ready = j;
                 }
+            };
+            auto issue_s = [&](int a, int j) {
+                ensure_k(j);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t q_addr = smem_u32(smem + kOffQ + a * kTileBytes);
+                const uint32_t k_addr = smem_u32(smem + kOffK + (j & 1) * kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc_mma(tmem + kColS + 128 * a, smem_desc_sw128(q_addr + off, 16, 1024),
+                           smem_desc_sw128(k_addr + off, 16, 1024), kIdescQK, kk > 0);
+                }
+                tc_commit(&bars->s_full[a]);
+            };
+            auto issue_pv = [&](int a, int j) {
+                if (ok) ok = mbar_wait(&bars->p_full[a], j & 1);
+                ensure_v(j);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t v_addr = smem_u32(smem + kOffV + (j & 1) * kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    // P: 16 keys = 8 packed columns per step.  V: MN-major; 16 keys =
+                    // 2 swizzle atoms (2048 B), second 64 dims 16 KB (LBO) away.
+                    tc_mma_tmem_a(tmem + kColO + 128 * a, tmem + kColS + 128 * a + 8 * kk,
+                                  smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), kIdescPV,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            if (ok) {
+                issue_s(0, 0);
+                if (last_tile[1] >= 0) issue_s(1, 0);
+                if (ok) tc_commit(&bars->k_empty[0]);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                for (int a = 0; a < kQTiles && ok; ++a) {
+                    if (j > last_tile[a]) continue;
+                    issue_pv(a, j);
+                    if (!ok) break;
+                    if (j == last_tile[a]) tc_commit(&bars->o_full[a]);
+                    else issue_s(a, j + 1);
+                }
+                if (!ok) break;
+                tc_commit(&bars->v_empty[j & 1]);
+                if (j + 1 < n_kv) tc_commit(&bars->k_empty[(j + 1) & 1]);
             }
             if (!ok) record_failure(bars, p.err_count);
         }
     } else {
         // --------------------------------------------------------- softmax
-        const int row = warp * 32 + lane;                 // TMEM lane = query row in tile
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const int a = warp >> 2;                          // query tile of this warpgroup
+        const int row = (warp & 3) * 32 + lane;           // TMEM lane = row within the tile
+        const int last = last_tile[a];
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t col_s = kColS + 128 * a, col_o = kColO + 128 * a;
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int sb = j & 1;
-            if (!mbar_wait(&bars->s_full[sb], (j >> 1) & 1)) {
+        bool ok = last >= 0;
+        for (int j = 0; ok && j <= last; ++j) {
+            if (!mbar_wait(&bars->s_full[a], j & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float s[128];
+            // Pass 1: row max over the 128 scores, 32 columns at a time.  Only
+            // the diagonal tile masks (key c > row); the others pay nothing.
+            const bool diag = j == last;
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + (sb ? kColS1 : kColS0) + c * 32, r);
-                tmem_wait_ld();
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            if (!diag) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col_s + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(r[e]));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col_s + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (c * 32 + e <= row) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(r[e]));
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->s_free[sb]);
-            if (j == n_kv - 1) {
-                // Diagonal tile (query and key tiles both start at q0): key c
-                // is visible to row `row` iff c <= row.
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > row) s[c] = -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
             const bool rescale = m_new > m_used + kRescaleThreshold;
@@ -305,78 +362,97 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 alpha = fast_exp2(m_used - m_new);      // 0 on the first tile
                 m_used = m_new;
             }
-            float sum = 0.f;
-            uint32_t pk[64];
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                // PV_a,j-1 has completed: the commit behind s_full covered it.
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(fmaf(s[2 * c], sl2, -m_used));
-                const float p1 = fast_exp2(fmaf(s[2 * c + 1], sl2, -m_used));
-                sum += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-            }
-            l = fmaf(l, alpha, sum);
-            if (j >= 1) {
-                // O and the P buffer are busy until PV_{j-1} completes.
-                if (!mbar_wait(&bars->pv_done, (j - 1) & 1)) {
-                    ok = false;
-                    break;
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col_o + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(lane_addr + col_o + c * 32, r);
                 }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+            }
+            // Pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs and
+            // written over the first 64 columns of S.  Chunk c's P columns
+            // [16c, 16c + 16) lie below its S columns [32c, 32c + 32), so a
+            // later chunk's scores are never overwritten before they are read.
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            const float neg_m = -m_used;
+            if (!diag) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_addr + kColO + c * 32, r);
-                        tmem_wait_ld();
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col_s + c * 32, r);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(lane_addr + kColO + c * 32, r);
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m));
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
                     }
-                    tmem_wait_st();
+                    tmem_st16(lane_addr + col_s + c * 16, pk);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col_s + c * 32, r);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int k0 = c * 32 + 2 * e;
+                        const float p0 = k0 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
+                        const float p1 = k0 + 1 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(lane_addr + col_s + c * 16, pk);
                 }
             }
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint8_t *dst = sP + (c >> 3) * kHalf + swz128(row, c & 7);
-                *reinterpret_cast<uint4 *>(dst) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
-            fence_proxy_async_smem();
+            tmem_wait_st();
+            l = fmaf(l, alpha, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
+            if (lane == 0) mbar_arrive(&bars->p_full[a]);
         }
-        if (ok && mbar_wait(&bars->pv_done, (n_kv - 1) & 1)) {
-            tc_fence_after();
-            const int qpos = q0 + row;
-            const float inv_l = 1.f / l;
-            uint16_t *orow = p.o + ((int64_t)(q_start + qpos) * p.Hq + h) * 128;
+        if (last >= 0) {
+            if (ok && mbar_wait(&bars->o_full[a], 0)) {
+                tc_fence_after();
+                const int qpos = q0 + a * kBM + row;
+                const float inv_l = 1.f / l;
+                uint16_t *orow = p.o + ((int64_t)(q_start + qpos) * p.Hq + h) * 128;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + kColO + c * 32, r);
-                tmem_wait_ld();
-                if (qpos < L) {
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col_o + c * 32, r);
+                    tmem_wait_ld();
+                    if (qpos < L) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[8 * e]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
-                        *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) = v;
+                        for (int e = 0; e < 4; ++e) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(r[8 * e]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
+                            *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) = v;
+                        }
                     }
                 }
+            } else {
+                record_failure(bars, p.err_count);
             }
-        } else {
-            record_failure(bars, p.err_count);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                      ::"r"(tmem), "r"(kTmemCols));
@@ -394,9 +470,9 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    const int n_qt = (p.max_seqlen_q + kBM - 1) / kBM;
-    if (p.B == 0 || n_qt == 0) return cudaSuccess;
-    dim3 grid(p.Hq, p.B, n_qt);
+    const int n_pairs = (p.max_seqlen_q + kQTiles * kBM - 1) / (kQTiles * kBM);
+    if (p.B == 0 || n_pairs == 0) return cudaSuccess;
+    dim3 grid(p.Hq, p.B, n_pairs);
     prefill_attn_kernel<<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(q_map, k_map, v_map, p);
     return cudaGetLastError();
 }
