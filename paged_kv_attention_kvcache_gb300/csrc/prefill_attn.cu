@@ -46,11 +46,12 @@ constexpr int kBN = 128;                        // keys per KV tile
 constexpr int kQTiles = 2;                      // query tiles per CTA
 constexpr int kHalf = 128 * 128;                // 128 rows x 64 dims x 2 B = 16 KB
 constexpr int kTileBytes = 2 * kHalf;           // one Q / K / V tile, 32 KB
-constexpr int kKVStages = 2;
+constexpr int kKStages = 2;                     // K ring depth
+constexpr int kVStages = 2;                     // V ring depth
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
-constexpr int kOffV = kOffK + kKVStages * kTileBytes;
-constexpr int kOffBar = kOffV + kKVStages * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kSoftmaxWarps = 4 * kQTiles;
 constexpr int kTmaWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
@@ -61,8 +62,8 @@ constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max 
 
 struct Barriers {
     uint64_t q_full;
-    uint64_t k_full[kKVStages], v_full[kKVStages];
-    uint64_t k_empty[kKVStages], v_empty[kKVStages];
+    uint64_t k_full[kKStages], v_full[kVStages];
+    uint64_t k_empty[kKStages], v_empty[kVStages];
     uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles];
     uint32_t tmem_base;
     int failed;
@@ -185,10 +186,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
-        for (int s = 0; s < kKVStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
         for (int a = 0; a < kQTiles; ++a) {
@@ -222,27 +225,36 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 tma_load_3d(sQ, &q_map, &bars->q_full, 0, h, row);
                 tma_load_3d(sQ + kHalf, &q_map, &bars->q_full, 64, h, row);
             }
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j & 1;
-                const uint32_t par = ((j >> 1) - 1) & 1;
-                const int row = k_start + j * kBN;
+            // K runs ahead of V: tile j's K is issued before tile j-1's V
+            // wait, so QK^T of the next tile never queues behind PV.
+            auto load_k = [&](int j) {
+                const int st = j % kKStages;
+                if (j >= kKStages &&
+                    !mbar_wait(&bars->k_empty[st], ((j / kKStages) - 1) & 1))
+                    return false;
                 uint8_t *sK = smem + kOffK + st * kTileBytes;
-                uint8_t *sV = smem + kOffV + st * kTileBytes;
-                if (j >= kKVStages && !mbar_wait(&bars->k_empty[st], par)) {
-                    record_failure(bars, p.err_count);
-                    break;
-                }
                 mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-                tma_load_3d(sK, &k_map, &bars->k_full[st], 0, kvh, row);
-                tma_load_3d(sK + kHalf, &k_map, &bars->k_full[st], 64, kvh, row);
-                if (j >= kKVStages && !mbar_wait(&bars->v_empty[st], par)) {
-                    record_failure(bars, p.err_count);
-                    break;
-                }
+                tma_load_3d(sK, &k_map, &bars->k_full[st], 0, kvh, k_start + j * kBN);
+                tma_load_3d(sK + kHalf, &k_map, &bars->k_full[st], 64, kvh, k_start + j * kBN);
+                return true;
+            };
+            auto load_v = [&](int j) {
+                const int st = j % kVStages;
+                if (j >= kVStages &&
+                    !mbar_wait(&bars->v_empty[st], ((j / kVStages) - 1) & 1))
+                    return false;
+                uint8_t *sV = smem + kOffV + st * kTileBytes;
                 mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                tma_load_3d(sV, &v_map, &bars->v_full[st], 0, kvh, row);
-                tma_load_3d(sV + kHalf, &v_map, &bars->v_full[st], 64, kvh, row);
+                tma_load_3d(sV, &v_map, &bars->v_full[st], 0, kvh, k_start + j * kBN);
+                tma_load_3d(sV + kHalf, &v_map, &bars->v_full[st], 64, kvh, k_start + j * kBN);
+                return true;
+            };
+            bool ok = load_k(0);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (j + 1 < n_kv) ok = load_k(j + 1);
+                if (ok) ok = load_v(j);
             }
+            if (!ok) record_failure(bars, p.err_count);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA
@@ -253,27 +265,33 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             int k_ready = -1, v_ready = -1;
             auto ensure_k = [&](int j) {
                 if (ok && k_ready < j) {
-                    ok = mbar_wait(&bars->k_full[j & 1], (j >> 1) & 1);
+                    ok = mbar_wait(&bars->k_full[j % kKStages], (j / kKStages) & 1);
                     k_ready = j;
                 }
             };
             auto ensure_v = [&](int j) {
                 if (ok && v_ready < j) {
-                    ok = mbar_wait(&bars->v_full[j & 1], (j >> 1) & 1);
+                    ok = mbar_wait(&bars->v_full[j % kVStages], (j / kVStages) & 1);
                     v_ready = j;
                 }
             };
+            // Descriptors are built once per operand tile; each K=16 step only
+            // adds a compile-time offset to the start-address field (shared
+            // addresses are < 256 KB, so that 14-bit field never carries).
+            // Rebuilding them per instruction costs the single issuing thread
+            // ~30 cycles per MMA, about half the tensor core's 64.
             auto issue_s = [&](int a, int j) {
                 ensure_k(j);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t q_addr = smem_u32(smem + kOffQ + a * kTileBytes);
-                const uint32_t k_addr = smem_u32(smem + kOffK + (j & 1) * kTileBytes);
+                const uint64_t dq = smem_desc_sw128(smem_u32(smem + kOffQ + a * kTileBytes), 16, 1024);
+                const uint64_t dk = smem_desc_sw128(
+                    smem_u32(smem + kOffK + (j % kKStages) * kTileBytes), 16, 1024);
+                const uint32_t d = tmem + kColS + 128 * a;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc_mma(tmem + kColS + 128 * a, smem_desc_sw128(q_addr + off, 16, 1024),
-                           smem_desc_sw128(k_addr + off, 16, 1024), kIdescQK, kk > 0);
+                    const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                    tc_mma(d, dq + off, dk + off, kIdescQK, kk > 0);
                 }
                 tc_commit(&bars->s_full[a]);
             };
@@ -282,15 +300,16 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 ensure_v(j);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t v_addr = smem_u32(smem + kOffV + (j & 1) * kTileBytes);
+                // P: 16 keys = 8 packed TMEM columns per step.  V: MN-major; 16
+                // keys = 2 swizzle atoms (2048 B) per step, the second 64 dims
+                // 16 KB (LBO) away.
+                const uint64_t dv = smem_desc_sw128(
+                    smem_u32(smem + kOffV + (j % kVStages) * kTileBytes), kHalf, 1024);
+                const uint32_t d = tmem + kColO + 128 * a, pa = tmem + kColS + 128 * a;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // P: 16 keys = 8 packed columns per step.  V: MN-major; 16 keys =
-                    // 2 swizzle atoms (2048 B), second 64 dims 16 KB (LBO) away.
-                    tc_mma_tmem_a(tmem + kColO + 128 * a, tmem + kColS + 128 * a + 8 * kk,
-                                  smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), kIdescPV,
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_tmem_a(d, pa + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV,
                                   (j > 0 || kk > 0) ? 1u : 0u);
-                }
             };
             if (ok) {
                 issue_s(0, 0);
@@ -306,8 +325,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     else issue_s(a, j + 1);
                 }
                 if (!ok) break;
-                tc_commit(&bars->v_empty[j & 1]);
-                if (j + 1 < n_kv) tc_commit(&bars->k_empty[(j + 1) & 1]);
+                tc_commit(&bars->v_empty[j % kVStages]);
+                if (j + 1 < n_kv) tc_commit(&bars->k_empty[(j + 1) % kKStages]);
             }
             if (!ok) record_failure(bars, p.err_count);
         }
