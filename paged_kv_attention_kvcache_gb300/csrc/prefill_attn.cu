@@ -91,27 +91,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+// Warp-collective forms: every lane of the warp executes them with the same
+// operands and elect.sync picks one lane to issue, so the operands stay
+// warp-uniform and the issuing loop runs without divergence.
+__device__ __forceinline__ void tc_mma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
-// Same with A (M x K, K-major, packed bf16 pairs per 32-bit column) read
-// from tensor memory at column address a_tmem.
-__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma_tmem_a_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(smem_u32(bar)) : "memory");
+__device__ __forceinline__ void tc_commit_elect(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -258,20 +264,26 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA
-        if (lane == 0) {
+        // The whole warp runs this loop (uniform control flow); elect.sync
+        // inside each tcgen05 instruction picks the issuing lane.
+        {
             constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
             constexpr uint32_t kIdescPV = idesc_bf16(kBM, 128, true);
-            bool ok = mbar_wait(&bars->q_full, 0);
+            // Waits are taken by every lane; the shuffle keeps `ok` uniform.
+            auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+                return __shfl_sync(0xffffffffu, (int)mbar_wait(bar, parity), 0) != 0;
+            };
+            bool ok = wait_all(&bars->q_full, 0);
             int k_ready = -1, v_ready = -1;
             auto ensure_k = [&](int j) {
                 if (ok && k_ready < j) {
-                    ok = mbar_wait(&bars->k_full[j % kKStages], (j / kKStages) & 1);
+                    ok = wait_all(&bars->k_full[j % kKStages], (j / kKStages) & 1);
                     k_ready = j;
                 }
             };
             auto ensure_v = [&](int j) {
                 if (ok && v_ready < j) {
-                    ok = mbar_wait(&bars->v_full[j % kVStages], (j / kVStages) & 1);
+                    ok = wait_all(&bars->v_full[j % kVStages], (j / kVStages) & 1);
                     v_ready = j;
                 }
             };
@@ -291,12 +303,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-                    tc_mma(d, dq + off, dk + off, kIdescQK, kk > 0);
+                    tc_mma_elect(d, dq + off, dk + off, kIdescQK, kk > 0);
                 }
-                tc_commit(&bars->s_full[a]);
+                tc_commit_elect(&bars->s_full[a]);
             };
             auto issue_pv = [&](int a, int j) {
-                if (ok) ok = mbar_wait(&bars->p_full[a], j & 1);
+                if (ok) ok = wait_all(&bars->p_full[a], j & 1);
                 ensure_v(j);
                 if (!ok) return;
                 tc_fence_after();
@@ -308,27 +320,27 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 const uint32_t d = tmem + kColO + 128 * a, pa = tmem + kColS + 128 * a;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_tmem_a(d, pa + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_tmem_a_elect(d, pa + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4),
+                                        kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
             };
             if (ok) {
                 issue_s(0, 0);
                 if (last_tile[1] >= 0) issue_s(1, 0);
-                if (ok) tc_commit(&bars->k_empty[0]);
+                if (ok) tc_commit_elect(&bars->k_empty[0]);
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 for (int a = 0; a < kQTiles && ok; ++a) {
                     if (j > last_tile[a]) continue;
                     issue_pv(a, j);
                     if (!ok) break;
-                    if (j == last_tile[a]) tc_commit(&bars->o_full[a]);
+                    if (j == last_tile[a]) tc_commit_elect(&bars->o_full[a]);
                     else issue_s(a, j + 1);
                 }
                 if (!ok) break;
-                tc_commit(&bars->v_empty[j % kVStages]);
-                if (j + 1 < n_kv) tc_commit(&bars->k_empty[(j + 1) % kKStages]);
+                tc_commit_elect(&bars->v_empty[j % kVStages]);
+                if (j + 1 < n_kv) tc_commit_elect(&bars->k_empty[(j + 1) % kKStages]);
             }
-            if (!ok) record_failure(bars, p.err_count);
+            if (!ok && lane == 0) record_failure(bars, p.err_count);
         }
     } else {
         // --------------------------------------------------------- softmax
