@@ -158,6 +158,35 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 lanes per instruction: (a0, a1) * (b, b) + (c, c).
+__device__ __forceinline__ float2 ffma2(float a0, float a1, float b, float c) {
+    uint64_t x, y, z, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(z) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t x, y, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
 __device__ __forceinline__ void record_failure(Barriers *bars, int *err_count) {
     if (atomicExch(&bars->failed, 1) == 0) flag_pipeline_failure(err_count);
 }
@@ -371,7 +400,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     tmem_ld32(lane_addr + col_s + c * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(r[e]));
+                    for (int e = 0; e < 16; ++e)
+                        mx8[e & 7] = fmax3(mx8[e & 7], __uint_as_float(r[2 * e]),
+                                           __uint_as_float(r[2 * e + 1]));
                 }
             } else {
 #pragma unroll
@@ -411,6 +442,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             // [16c, 16c + 16) lie below its S columns [32c, 32c + 32), so a
             // later chunk's scores are never overwritten before they are read.
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             const float neg_m = -m_used;
             if (!diag) {
 #pragma unroll
@@ -421,10 +453,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m));
-                        sum4[e & 3] += p0 + p1;
-                        pk[e] = pack_bf16x2(p0, p1);
+                        const float2 x = ffma2(__uint_as_float(r[2 * e]),
+                                               __uint_as_float(r[2 * e + 1]), sl2, neg_m);
+                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        sum2[e & 1] = fadd2(sum2[e & 1], pp);
+                        pk[e] = pack_bf16x2(pp.x, pp.y);
                     }
                     tmem_st16(lane_addr + col_s + c * 16, pk);
                 }
@@ -447,7 +480,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
             }
             tmem_wait_st();
-            l = fmaf(l, alpha, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            l = fmaf(l, alpha, ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3])) +
+                                   ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->p_full[a]);
