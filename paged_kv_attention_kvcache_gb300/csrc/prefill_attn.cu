@@ -394,15 +394,19 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             if (!diag) {
+                // The next chunk's load is in flight while this one is reduced.
+                uint32_t rb[2][32];
+                tmem_ld32(lane_addr + col_s, rb[0]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col_s + c * 32, r);
-                    tmem_wait_ld();
+                    if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                    const uint32_t (&r)[32] = rb[c & 1];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         mx8[e & 7] = fmax3(mx8[e & 7], __uint_as_float(r[2 * e]),
                                            __uint_as_float(r[2 * e + 1]));
+                    if (c < 3) tmem_wait_ld();
                 }
             } else {
 #pragma unroll
@@ -445,11 +449,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             const float neg_m = -m_used;
             if (!diag) {
+                uint32_t rb[2][32];
+                tmem_ld32(lane_addr + col_s, rb[0]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col_s + c * 32, r);
-                    tmem_wait_ld();
+                    // Chunk c + 1's scores (columns 32c + 32 ..) are loaded before
+                    // chunk c's P is stored over columns 16c .. 16c + 15.
+                    if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                    const uint32_t (&r)[32] = rb[c & 1];
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -459,6 +467,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         sum2[e & 1] = fadd2(sum2[e & 1], pp);
                         pk[e] = pack_bf16x2(pp.x, pp.y);
                     }
+                    if (c < 3) tmem_wait_ld();
                     tmem_st16(lane_addr + col_s + c * 16, pk);
                 }
             } else {
