@@ -337,8 +337,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 tc_commit_elect(&bars->s_full[a]);
             };
             auto issue_pv = [&](int a, int j) {
-                if (ok) ok = wait_all(&bars->p_full[a], j & 1);
+                // V_j (and K_j+1 for the S that follows) were loaded long ago;
+                // confirm them before waiting for P so that these barrier round
+                // trips stay off the softmax -> PV -> S critical path.
                 ensure_v(j);
+                if (j + 1 <= last_tile[a]) ensure_k(j + 1);
+                if (ok) ok = wait_all(&bars->p_full[a], j & 1);
                 if (!ok) return;
                 tc_fence_after();
                 // P: 16 keys = 8 packed TMEM columns per step.  V: MN-major; 16
