@@ -61,13 +61,45 @@ constexpr uint32_t kColS = 0, kColO = 256;      // S_a at kColS + 128a, O_a at k
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
 
 struct Barriers {
-    uint64_t q_full;
+    uint64_t q_full, q_empty;
     uint64_t k_full[kKStages], v_full[kVStages];
     uint64_t k_empty[kKStages], v_empty[kVStages];
-    uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles];
+    uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles], o_empty[kQTiles];
     uint32_t tmem_base;
     int failed;
 };
+
+// One unit of work: a pair of 128-row query tiles of one head of one
+// sequence.  Items are numbered heaviest first (pair index descending, then
+// sequence, then head, so the heads sharing a kv head are adjacent).
+struct Item {
+    int h, q_start, L, k_start, q0, kvh;
+    int last[kQTiles];      // last key tile of query tile a (-1: tile has no rows)
+    int n_kv;               // key tiles the pair needs
+};
+
+__device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n_pairs, Item &it) {
+    const int h = w % p.Hq;
+    const int t = w / p.Hq;
+    const int b = t % p.B;
+    const int pair = n_pairs - 1 - t / p.B;
+    const int q_start = __ldg(p.cu_seqlens_q + b);
+    const int L = __ldg(p.cu_seqlens_q + b + 1) - q_start;
+    const int q0 = pair * kQTiles * kBM;
+    if (q0 >= L) return false;
+    const int qt0 = pair * kQTiles;
+    const bool has1 = q0 + kBM < L;
+    it.h = h;
+    it.q_start = q_start;
+    it.L = L;
+    it.k_start = __ldg(p.cu_seqlens_k + b);
+    it.q0 = q0;
+    it.kvh = h / (p.Hq / p.Hkv);
+    it.last[0] = qt0;
+    it.last[1] = has1 ? qt0 + 1 : -1;
+    it.n_kv = has1 ? qt0 + 2 : qt0 + 1;
+    return true;
+}
 constexpr int kPrefillSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
 
 // ------------------------------------------------------------ tcgen05 PTX
@@ -196,23 +228,11 @@ __device__ __forceinline__ void record_failure(Barriers *bars, int *err_count) {
 __global__ void __launch_bounds__(kPrefillThreads, 1)
 prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap k_map,
-                    const __grid_constant__ CUtensorMap v_map, const PrefillParams p) {
-    const int h = blockIdx.x, b = blockIdx.y;
-    const int pair = (int)gridDim.z - 1 - (int)blockIdx.z;  // heaviest pairs first
-    const int q_start = __ldg(p.cu_seqlens_q + b);
-    const int L = __ldg(p.cu_seqlens_q + b + 1) - q_start;
-    const int k_start = __ldg(p.cu_seqlens_k + b);
-    const int q0 = pair * kQTiles * kBM;
-    if (q0 >= L) return;                                    // uniform across the CTA
+                    const __grid_constant__ CUtensorMap v_map, const PrefillParams p,
+                    int n_pairs, int n_items) {
     if (pipeline_failed_before(p.err_count)) return;
-    // Query tile a holds rows [q0 + 128a, q0 + 128a + 128) and, by causality,
-    // needs key tiles 0 .. qt0 + a; tile 1 may hold no row of this sequence.
-    const int qt0 = pair * kQTiles;
-    const bool has1 = q0 + kBM < L;
-    const int last_tile[2] = {qt0, has1 ? qt0 + 1 : -1};
-    const int n_kv = has1 ? qt0 + 2 : qt0 + 1;
-    const int kvh = h / (p.Hq / p.Hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float sl2 = p.scale_log2;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -221,6 +241,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
@@ -233,6 +254,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&bars->s_full[a], 1);
             mbar_init(&bars->p_full[a], 4);
             mbar_init(&bars->o_full[a], 1);
+            mbar_init(&bars->o_empty[a], 4);
         }
         bars->failed = 0;
         fence_mbarrier_init();
@@ -253,41 +275,56 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             tma_prefetch_desc(&q_map);
             tma_prefetch_desc(&k_map);
             tma_prefetch_desc(&v_map);
-            mbar_arrive_expect_tx(&bars->q_full, has1 ? 2 * kTileBytes : kTileBytes);
-            for (int a = 0; a < (has1 ? 2 : 1); ++a) {
-                uint8_t *sQ = smem + kOffQ + a * kTileBytes;
-                const int row = q_start + q0 + a * kBM;
-                tma_load_3d(sQ, &q_map, &bars->q_full, 0, h, row);
-                tma_load_3d(sQ + kHalf, &q_map, &bars->q_full, 64, h, row);
-            }
-            // K runs ahead of V: tile j's K is issued before tile j-1's V
-            // wait, so QK^T of the next tile never queues behind PV.
-            auto load_k = [&](int j) {
-                const int st = j % kKStages;
-                if (j >= kKStages &&
-                    !mbar_wait(&bars->k_empty[st], ((j / kKStages) - 1) & 1))
+            int qcnt = 0, kcnt = 0, vcnt = 0;
+            bool ok = true;
+            // K runs one tile ahead of V, so QK^T of the next tile never waits
+            // behind PV; the next item's Q and first K load while the current
+            // item drains.
+            auto load_k = [&](const Item &it, int j) {
+                const int st = kcnt % kKStages;
+                if (kcnt >= kKStages &&
+                    !mbar_wait(&bars->k_empty[st], ((kcnt / kKStages) - 1) & 1))
                     return false;
                 uint8_t *sK = smem + kOffK + st * kTileBytes;
                 mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-                tma_load_3d(sK, &k_map, &bars->k_full[st], 0, kvh, k_start + j * kBN);
-                tma_load_3d(sK + kHalf, &k_map, &bars->k_full[st], 64, kvh, k_start + j * kBN);
+                tma_load_3d(sK, &k_map, &bars->k_full[st], 0, it.kvh, it.k_start + j * kBN);
+                tma_load_3d(sK + kHalf, &k_map, &bars->k_full[st], 64, it.kvh, it.k_start + j * kBN);
+                ++kcnt;
                 return true;
             };
-            auto load_v = [&](int j) {
-                const int st = j % kVStages;
-                if (j >= kVStages &&
-                    !mbar_wait(&bars->v_empty[st], ((j / kVStages) - 1) & 1))
+            auto load_v = [&](const Item &it, int j) {
+                const int st = vcnt % kVStages;
+                if (vcnt >= kVStages &&
+                    !mbar_wait(&bars->v_empty[st], ((vcnt / kVStages) - 1) & 1))
                     return false;
                 uint8_t *sV = smem + kOffV + st * kTileBytes;
                 mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                tma_load_3d(sV, &v_map, &bars->v_full[st], 0, kvh, k_start + j * kBN);
-                tma_load_3d(sV + kHalf, &v_map, &bars->v_full[st], 64, kvh, k_start + j * kBN);
+                tma_load_3d(sV, &v_map, &bars->v_full[st], 0, it.kvh, it.k_start + j * kBN);
+                tma_load_3d(sV + kHalf, &v_map, &bars->v_full[st], 64, it.kvh, it.k_start + j * kBN);
+                ++vcnt;
                 return true;
             };
-            bool ok = load_k(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) ok = load_k(j + 1);
-                if (ok) ok = load_v(j);
+            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+                Item it;
+                if (!decode_item(w, p, n_pairs, it)) continue;
+                const bool has1 = it.last[1] >= 0;
+                if (qcnt >= 1 && !mbar_wait(&bars->q_empty, (qcnt - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars->q_full, has1 ? 2 * kTileBytes : kTileBytes);
+                for (int a = 0; a < (has1 ? 2 : 1); ++a) {
+                    uint8_t *sQ = smem + kOffQ + a * kTileBytes;
+                    const int row = it.q_start + it.q0 + a * kBM;
+                    tma_load_3d(sQ, &q_map, &bars->q_full, 0, it.h, row);
+                    tma_load_3d(sQ + kHalf, &q_map, &bars->q_full, 64, it.h, row);
+                }
+                ++qcnt;
+                ok = load_k(it, 0);
+                for (int j = 0; ok && j < it.n_kv; ++j) {
+                    if (j + 1 < it.n_kv) ok = load_k(it, j + 1);
+                    if (ok) ok = load_v(it, j);
+                }
             }
             if (!ok) record_failure(bars, p.err_count);
         }
@@ -295,39 +332,51 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         // ------------------------------------------------------------- MMA
         // The whole warp runs this loop (uniform control flow); elect.sync
         // inside each tcgen05 instruction picks the issuing lane.
-        {
-            constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
-            constexpr uint32_t kIdescPV = idesc_bf16(kBM, 128, true);
-            // Waits are taken by every lane; the shuffle keeps `ok` uniform.
-            auto wait_all = [&](uint64_t *bar, uint32_t parity) {
-                return __shfl_sync(0xffffffffu, (int)mbar_wait(bar, parity), 0) != 0;
-            };
-            bool ok = wait_all(&bars->q_full, 0);
+        constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
+        constexpr uint32_t kIdescPV = idesc_bf16(kBM, 128, true);
+        // Waits are taken by every lane; the shuffle keeps `ok` uniform.
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+            return __shfl_sync(0xffffffffu, (int)mbar_wait(bar, parity), 0) != 0;
+        };
+        bool ok = true;
+        int qcnt = 0, kcnt = 0, vcnt = 0;        // tiles consumed so far
+        int pcnt[kQTiles] = {0, 0}, ocnt[kQTiles] = {0, 0};
+        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            Item it;
+            if (!decode_item(w, p, n_pairs, it)) continue;
+            const bool has1 = it.last[1] >= 0;
+            ok = wait_all(&bars->q_full, qcnt & 1);
+            ++qcnt;
+            // Key tile j of this item is ring slot kbase + j (same for V).
+            const int kbase = kcnt, vbase = vcnt;
             int k_ready = -1, v_ready = -1;
+            int s_left = (it.last[0] + 1) + (has1 ? it.last[1] + 1 : 0);
             auto ensure_k = [&](int j) {
                 if (ok && k_ready < j) {
-                    ok = wait_all(&bars->k_full[j % kKStages], (j / kKStages) & 1);
+                    const int c = kbase + j;
+                    ok = wait_all(&bars->k_full[c % kKStages], (c / kKStages) & 1);
                     k_ready = j;
                 }
             };
             auto ensure_v = [&](int j) {
                 if (ok && v_ready < j) {
-                    ok = wait_all(&bars->v_full[j % kVStages], (j / kVStages) & 1);
+                    const int c = vbase + j;
+                    ok = wait_all(&bars->v_full[c % kVStages], (c / kVStages) & 1);
                     v_ready = j;
                 }
             };
             // Descriptors are built once per operand tile; each K=16 step only
             // adds a compile-time offset to the start-address field (shared
             // addresses are < 256 KB, so that 14-bit field never carries).
-            // Rebuilding them per instruction costs the single issuing thread
-            // ~30 cycles per MMA, about half the tensor core's 64.
+            // Rebuilding them per instruction costs the issuing warp ~30 cycles
+            // per MMA, about half the tensor core's 64.
             auto issue_s = [&](int a, int j) {
                 ensure_k(j);
                 if (!ok) return;
                 tc_fence_after();
                 const uint64_t dq = smem_desc_sw128(smem_u32(smem + kOffQ + a * kTileBytes), 16, 1024);
                 const uint64_t dk = smem_desc_sw128(
-                    smem_u32(smem + kOffK + (j % kKStages) * kTileBytes), 16, 1024);
+                    smem_u32(smem + kOffK + ((kbase + j) % kKStages) * kTileBytes), 16, 1024);
                 const uint32_t d = tmem + kColS + 128 * a;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -335,197 +384,217 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     tc_mma_elect(d, dq + off, dk + off, kIdescQK, kk > 0);
                 }
                 tc_commit_elect(&bars->s_full[a]);
+                // After the item's last QK^T the Q buffer may be refilled.
+                if (--s_left == 0) tc_commit_elect(&bars->q_empty);
             };
             auto issue_pv = [&](int a, int j) {
                 // V_j (and K_j+1 for the S that follows) were loaded long ago;
                 // confirm them before waiting for P so that these barrier round
                 // trips stay off the softmax -> PV -> S critical path.
                 ensure_v(j);
-                if (j + 1 <= last_tile[a]) ensure_k(j + 1);
-                if (ok) ok = wait_all(&bars->p_full[a], j & 1);
+                if (j + 1 <= it.last[a]) ensure_k(j + 1);
+                if (ok && j == 0 && ocnt[a] >= 1)     // epilogue of the previous item done
+                    ok = wait_all(&bars->o_empty[a], (ocnt[a] - 1) & 1);
+                if (ok) ok = wait_all(&bars->p_full[a], pcnt[a] & 1);
                 if (!ok) return;
+                ++pcnt[a];
                 tc_fence_after();
                 // P: 16 keys = 8 packed TMEM columns per step.  V: MN-major; 16
                 // keys = 2 swizzle atoms (2048 B) per step, the second 64 dims
                 // 16 KB (LBO) away.
                 const uint64_t dv = smem_desc_sw128(
-                    smem_u32(smem + kOffV + (j % kVStages) * kTileBytes), kHalf, 1024);
+                    smem_u32(smem + kOffV + ((vbase + j) % kVStages) * kTileBytes), kHalf, 1024);
                 const uint32_t d = tmem + kColO + 128 * a, pa = tmem + kColS + 128 * a;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_tmem_a_elect(d, pa + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4),
                                         kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
             };
-            if (ok) {
-                issue_s(0, 0);
-                if (last_tile[1] >= 0) issue_s(1, 0);
-                if (ok) tc_commit_elect(&bars->k_empty[0]);
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
+            issue_s(0, 0);
+            if (has1) issue_s(1, 0);
+            if (ok) tc_commit_elect(&bars->k_empty[kbase % kKStages]);
+            for (int j = 0; ok && j < it.n_kv; ++j) {
                 for (int a = 0; a < kQTiles && ok; ++a) {
-                    if (j > last_tile[a]) continue;
+                    if (j > it.last[a]) continue;
                     issue_pv(a, j);
                     if (!ok) break;
-                    if (j == last_tile[a]) tc_commit_elect(&bars->o_full[a]);
-                    else issue_s(a, j + 1);
+                    if (j == it.last[a]) {
+                        tc_commit_elect(&bars->o_full[a]);
+                        ++ocnt[a];
+                    } else {
+                        issue_s(a, j + 1);
+                    }
                 }
                 if (!ok) break;
-                tc_commit_elect(&bars->v_empty[j % kVStages]);
-                if (j + 1 < n_kv) tc_commit_elect(&bars->k_empty[(j + 1) % kKStages]);
+                tc_commit_elect(&bars->v_empty[(vbase + j) % kVStages]);
+                if (j + 1 < it.n_kv) tc_commit_elect(&bars->k_empty[(kbase + j + 1) % kKStages]);
             }
-            if (!ok && lane == 0) record_failure(bars, p.err_count);
+            kcnt += it.n_kv;
+            vcnt += it.n_kv;
         }
+        if (!ok && lane == 0) record_failure(bars, p.err_count);
     } else {
         // --------------------------------------------------------- softmax
         const int a = warp >> 2;                          // query tile of this warpgroup
         const int row = (warp & 3) * 32 + lane;           // TMEM lane = row within the tile
-        const int last = last_tile[a];
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t col_s = kColS + 128 * a, col_o = kColO + 128 * a;
-        const float sl2 = p.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
-        bool ok = last >= 0;
-        for (int j = 0; ok && j <= last; ++j) {
-            if (!mbar_wait(&bars->s_full[a], j & 1)) {
+        bool ok = true;
+        int scnt = 0, ocnt = 0;
+        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            Item it;
+            if (!decode_item(w, p, n_pairs, it)) continue;
+            const int last = it.last[a];
+            if (last < 0) continue;                       // this query tile has no rows
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; ok && j <= last; ++j) {
+                if (!mbar_wait(&bars->s_full[a], scnt & 1)) {
+                    ok = false;
+                    break;
+                }
+                ++scnt;
+                tc_fence_after();
+                // Pass 1: row max over the 128 scores, 32 columns at a time.  Only
+                // the diagonal tile masks (key c > row); the others pay nothing.
+                const bool diag = j == last;
+                float mx8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+                if (!diag) {
+                    // The next chunk's load is in flight while this one is reduced.
+                    uint32_t rb[2][32];
+                    tmem_ld32(lane_addr + col_s, rb[0]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                        const uint32_t (&r)[32] = rb[c & 1];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            mx8[e & 7] = fmax3(mx8[e & 7], __uint_as_float(r[2 * e]),
+                                               __uint_as_float(r[2 * e + 1]));
+                        if (c < 3) tmem_wait_ld();
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + col_s + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c * 32 + e <= row) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(r[e]));
+                    }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float m_new = fmaxf(m_used, mx * sl2);
+                float alpha = 1.f;
+                const bool rescale = m_new > m_used + kRescaleThreshold;
+                if (rescale) {
+                    alpha = fast_exp2(m_used - m_new);      // 0 on the first tile
+                    m_used = m_new;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                    // PV_a,j-1 has completed: the commit behind s_full covered it.
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + col_o + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(lane_addr + col_o + c * 32, r);
+                    }
+                }
+                // Pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs and
+                // written over the first 64 columns of S.  Chunk c's P columns
+                // [16c, 16c + 16) lie below its S columns [32c, 32c + 32), so a
+                // later chunk's scores are never overwritten before they are read.
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float neg_m = -m_used;
+                if (!diag) {
+                    uint32_t rb[2][32];
+                    tmem_ld32(lane_addr + col_s, rb[0]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        // Chunk c + 1's scores (columns 32c + 32 ..) are loaded before
+                        // chunk c's P is stored over columns 16c .. 16c + 15.
+                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                        const uint32_t (&r)[32] = rb[c & 1];
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 x = ffma2(__uint_as_float(r[2 * e]),
+                                                   __uint_as_float(r[2 * e + 1]), sl2, neg_m);
+                            const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                            sum2[e & 1] = fadd2(sum2[e & 1], pp);
+                            pk[e] = pack_bf16x2(pp.x, pp.y);
+                        }
+                        if (c < 3) tmem_wait_ld();
+                        tmem_st16(lane_addr + col_s + c * 16, pk);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + col_s + c * 32, r);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int k0 = c * 32 + 2 * e;
+                            const float p0 = k0 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
+                            const float p1 = k0 + 1 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
+                            sum4[e & 3] += p0 + p1;
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(lane_addr + col_s + c * 16, pk);
+                    }
+                }
+                tmem_wait_st();
+                l = fmaf(l, alpha, ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3])) +
+                                       ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full[a]);
+            }
+            if (!ok) break;
+            if (!mbar_wait(&bars->o_full[a], ocnt & 1)) {
                 ok = false;
                 break;
             }
+            ++ocnt;
             tc_fence_after();
-            // Pass 1: row max over the 128 scores, 32 columns at a time.  Only
-            // the diagonal tile masks (key c > row); the others pay nothing.
-            const bool diag = j == last;
-            float mx8[8];
+            const int qpos = it.q0 + a * kBM + row;
+            const float inv_l = 1.f / l;
+            uint16_t *orow = p.o + ((int64_t)(it.q_start + qpos) * p.Hq + it.h) * 128;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-            if (!diag) {
-                // The next chunk's load is in flight while this one is reduced.
-                uint32_t rb[2][32];
-                tmem_ld32(lane_addr + col_s, rb[0]);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_addr + col_o + c * 32, r);
                 tmem_wait_ld();
+                if (qpos < it.L) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
-                    const uint32_t (&r)[32] = rb[c & 1];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        mx8[e & 7] = fmax3(mx8[e & 7], __uint_as_float(r[2 * e]),
-                                           __uint_as_float(r[2 * e + 1]));
-                    if (c < 3) tmem_wait_ld();
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col_s + c * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c * 32 + e <= row) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(r[e]));
-                }
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_new = fmaxf(m_used, mx * sl2);
-            float alpha = 1.f;
-            const bool rescale = m_new > m_used + kRescaleThreshold;
-            if (rescale) {
-                alpha = fast_exp2(m_used - m_new);      // 0 on the first tile
-                m_used = m_new;
-            }
-            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-                // PV_a,j-1 has completed: the commit behind s_full covered it.
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col_o + c * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(lane_addr + col_o + c * 32, r);
-                }
-            }
-            // Pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs and
-            // written over the first 64 columns of S.  Chunk c's P columns
-            // [16c, 16c + 16) lie below its S columns [32c, 32c + 32), so a
-            // later chunk's scores are never overwritten before they are read.
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            const float neg_m = -m_used;
-            if (!diag) {
-                uint32_t rb[2][32];
-                tmem_ld32(lane_addr + col_s, rb[0]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    // Chunk c + 1's scores (columns 32c + 32 ..) are loaded before
-                    // chunk c's P is stored over columns 16c .. 16c + 15.
-                    if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
-                    const uint32_t (&r)[32] = rb[c & 1];
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 x = ffma2(__uint_as_float(r[2 * e]),
-                                               __uint_as_float(r[2 * e + 1]), sl2, neg_m);
-                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        sum2[e & 1] = fadd2(sum2[e & 1], pp);
-                        pk[e] = pack_bf16x2(pp.x, pp.y);
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(r[8 * e]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) = v;
                     }
-                    if (c < 3) tmem_wait_ld();
-                    tmem_st16(lane_addr + col_s + c * 16, pk);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col_s + c * 32, r);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int k0 = c * 32 + 2 * e;
-                        const float p0 = k0 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
-                        const float p1 = k0 + 1 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
-                        sum4[e & 3] += p0 + p1;
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st16(lane_addr + col_s + c * 16, pk);
                 }
             }
-            tmem_wait_st();
-            l = fmaf(l, alpha, ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3])) +
-                                   ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)));
+            // O_a may now be overwritten by the next item's first PV.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[a]);
+            if (lane == 0) mbar_arrive(&bars->o_empty[a]);
         }
-        if (last >= 0) {
-            if (ok && mbar_wait(&bars->o_full[a], 0)) {
-                tc_fence_after();
-                const int qpos = q0 + a * kBM + row;
-                const float inv_l = 1.f / l;
-                uint16_t *orow = p.o + ((int64_t)(q_start + qpos) * p.Hq + h) * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col_o + c * 32, r);
-                    tmem_wait_ld();
-                    if (qpos < L) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(r[8 * e]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
-                            v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
-                            v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
-                            v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
-                            *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) = v;
-                        }
-                    }
-                }
-            } else {
-                record_failure(bars, p.err_count);
-            }
-        }
+        if (!ok) record_failure(bars, p.err_count);
     }
 
     tc_fence_before();
@@ -550,8 +619,15 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
     }
     const int n_pairs = (p.max_seqlen_q + kQTiles * kBM - 1) / (kQTiles * kBM);
     if (p.B == 0 || n_pairs == 0) return cudaSuccess;
-    dim3 grid(p.Hq, p.B, n_pairs);
-    prefill_attn_kernel<<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(q_map, k_map, v_map, p);
+    const int64_t items = (int64_t)n_pairs * p.B * p.Hq;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    // Persistent: one CTA per SM, each walking items blockIdx.x, +grid, ...
+    const int grid = (int)(items < sms ? items : sms);
+    prefill_attn_kernel<<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(q_map, k_map, v_map, p,
+                                                                         n_pairs, (int)items);
     return cudaGetLastError();
 }
 
