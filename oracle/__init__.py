@@ -70,6 +70,10 @@ def _load():
             lib.orc_paged_decode.argtypes = [_P, _I64, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
                                              _I32, _I32, _I64, _F64, _P, _I64, _P]
             lib.orc_paged_decode.restype = _I32
+            lib.orc_attention_paged_prefill.argtypes = [_P, _I64, _P, _P, _P, _I32, _P, _P, _I32,
+                                                        _I32, _I32, _I32, _I32, _I64, _F64, _P,
+                                                        _I64, _P]
+            lib.orc_attention_paged_prefill.restype = _I32
             _lib = lib
     return _lib
 
@@ -230,4 +234,40 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, 
                                   _ptr(out))
     if rc:
         raise ValueError(f"orc_paged_decode failed: {rc}")
+    return out
+
+
+def attention_paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
+                            scale: float, rows=None):
+    """Prefill over the paged cache (prefix hit / chunked prefill).
+
+    q: [Tq, Hq, d] bf16 bits (the new tokens); caches [nb, bs, Hkv, d] bf16
+    bits holding each sequence's Lk keys (prefix + new) through block_tables
+    [B, MB] int32; cu_seqlens_q / cu_seqlens_k: [B+1] int32 (Lk >= Lq).
+    Query i of a sequence sees keys j <= Lk - Lq + i.  rows: optional [n, 2]
+    (token, head).  Returns [Tq, Hq, d] or [n, d] fp64.
+    """
+    q = _u16(q)
+    Tq, Hq, d = q.shape
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint16 or not c.flags.c_contiguous:
+            raise TypeError("caches must be contiguous bf16 bits")
+    nb, bs, Hkv, d2 = k_cache.shape
+    assert d2 == d
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cq = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    ck = np.ascontiguousarray(cu_seqlens_k, dtype=np.int32)
+    B = cq.size - 1
+    if rows is None:
+        out = np.empty((Tq, Hq, d), np.float64)
+        rp, n = None, 0
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 2)
+        out = np.empty((rows.shape[0], d), np.float64)
+        rp, n = rows, rows.shape[0]
+    rc = _load().orc_attention_paged_prefill(_ptr(q), Hq * d, _ptr(k_cache), _ptr(v_cache),
+                                             _ptr(bt), bt.shape[1], _ptr(cq), _ptr(ck), B, Hq,
+                                             Hkv, d, bs, nb, scale, _ptr(rp), n, _ptr(out))
+    if rc:
+        raise ValueError(f"orc_attention_paged_prefill failed: {rc}")
     return out

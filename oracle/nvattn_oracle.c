@@ -393,3 +393,82 @@ int orc_paged_decode(const uint16_t *q, int64_t q_stride,
     }
     return status;
 }
+
+/*
+ * [PAGED] + [ATTN] Prefill over the paged cache: a prefix-cache hit or a
+ * later chunk of chunked prefill ("3.3 Model skeleton and core operators",
+ * sec. 7.2: k, v are replaced by the whole cache and block_table is passed;
+ * "nano-vllm code walkthrough", Prefill stage case 2).  Sequence b has
+ * Lq = cu_q[b+1] - cu_q[b] new queries and Lk = cu_k[b+1] - cu_k[b] keys in
+ * the cache (prefix plus the new tokens, already stored); its logical K/V
+ * sequence is stitched block by block through block_tables[b].  Query i sits
+ * at position Lk - Lq + i and sees keys j <= Lk - Lq + i (causality aligned
+ * to the last key).  q is [Tq, Hq, d] with token stride q_stride; out is
+ * [Tq, Hq, d] (rows == NULL) or [n_rows, d].  Returns -3 on a block id
+ * outside [0, num_blocks) or Lk > max_blocks * block_size, -4 if Lk < Lq.
+ */
+int orc_attention_paged_prefill(const uint16_t *q, int64_t q_stride,
+                                const uint16_t *k_cache, const uint16_t *v_cache,
+                                const int32_t *block_tables, int max_blocks,
+                                const int32_t *cu_q, const int32_t *cu_k, int B,
+                                int Hq, int Hkv, int d, int block_size,
+                                int64_t num_blocks, double scale,
+                                const int64_t *rows, int64_t n_rows, double *out) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || block_size <= 0) return -1;
+    int group = Hq / Hkv;
+    int64_t Tq = B > 0 ? cu_q[B] : 0;
+    int64_t n_units = rows ? n_rows : Tq * Hq;
+    int64_t max_l = (int64_t)max_blocks * block_size;
+    int status = 0;
+#pragma omp parallel
+    {
+        uint16_t *k_seq = (uint16_t *)malloc((size_t)(max_l > 0 ? max_l : 1) * d * sizeof(uint16_t));
+        uint16_t *v_seq = (uint16_t *)malloc((size_t)(max_l > 0 ? max_l : 1) * d * sizeof(uint16_t));
+        const uint16_t **k_rows = (const uint16_t **)malloc((size_t)(max_l > 0 ? max_l : 1) * sizeof(void *));
+        const uint16_t **v_rows = (const uint16_t **)malloc((size_t)(max_l > 0 ? max_l : 1) * sizeof(void *));
+        double *scores = (double *)malloc((size_t)(max_l > 0 ? max_l : 1) * sizeof(double));
+        double *qv = (double *)malloc((size_t)d * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < n_units; ++u) {
+            int64_t t = rows ? rows[2 * u] : u / Hq;
+            int h = rows ? (int)rows[2 * u + 1] : (int)(u % Hq);
+            double *o = out + u * d;
+            int b = -1;
+            for (int s = 0; s < B; ++s)
+                if (t >= cu_q[s] && t < cu_q[s + 1]) { b = s; break; }
+            int64_t lq = b >= 0 ? (int64_t)cu_q[b + 1] - cu_q[b] : 0;
+            int64_t lk = b >= 0 ? (int64_t)cu_k[b + 1] - cu_k[b] : 0;
+            int bad = b < 0 || h < 0 || h >= Hq ? -2 : (lk > max_l ? -3 : (lk < lq ? -4 : 0));
+            if (bad) {
+                for (int i = 0; i < d; ++i) o[i] = NAN;
+#pragma omp atomic write
+                status = bad;
+                continue;
+            }
+            int64_t i_q = t - cu_q[b];
+            int64_t visible = i_q + (lk - lq) + 1;
+            int kvh = h / group;
+            int ok = 1;
+            for (int64_t j = 0; j < visible; ++j) {
+                int64_t blk = block_tables[(int64_t)b * max_blocks + j / block_size];
+                if (blk < 0 || blk >= num_blocks) { ok = 0; break; }
+                int64_t off = ((blk * block_size + j % block_size) * Hkv + kvh) * (int64_t)d;
+                memcpy(k_seq + j * d, k_cache + off, (size_t)d * sizeof(uint16_t));
+                memcpy(v_seq + j * d, v_cache + off, (size_t)d * sizeof(uint16_t));
+                k_rows[j] = k_seq + j * d;
+                v_rows[j] = v_seq + j * d;
+            }
+            if (!ok) {
+                for (int i = 0; i < d; ++i) o[i] = NAN;
+#pragma omp atomic write
+                status = -3;
+                continue;
+            }
+            const uint16_t *qrow = q + t * q_stride + (int64_t)h * d;
+            for (int i = 0; i < d; ++i) qv[i] = bf16_bits_to_double(qrow[i]);
+            dense_attention_row(qv, k_rows, v_rows, visible, d, scale, scores, o);
+        }
+        free(k_seq); free(v_seq); free(k_rows); free(v_rows); free(scores); free(qv);
+    }
+    return status;
+}

@@ -420,3 +420,55 @@ def test_paged_decode_empty_context_is_zero_and_pairs_subset():
     np.testing.assert_array_equal(sub, full[1, ::-1])
     with pytest.raises(ValueError):
         oracle.paged_decode(q, kc, vc, np.array([[2, 0], [5, -1]], np.int32), ctx, 0.3)
+
+
+# ---------------------------------------------- prefill over the paged cache
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2)])
+def test_paged_prefill_equals_contiguous_bottom_right_causal(hq, hkv):
+    # Prefix lengths and new-token counts per sequence; the cache holds all
+    # prefix + new keys in shuffled blocks of 4 tokens.
+    g = np.random.default_rng(40 + hq)
+    d, bs = 16, 4
+    prefix = np.array([0, 3, 8, 5])
+    new = np.array([5, 1, 4, 7])
+    lk = prefix + new
+    B = lk.size
+    nb = int(sum(math.ceil(int(x) / bs) for x in lk)) + 2
+    bt = wl.carve_block_tables(g.permutation(nb).astype(np.int32), lk, block_size=bs)
+    kc = bits(g.standard_normal((nb, bs, hkv, d)))
+    vc = bits(g.standard_normal((nb, bs, hkv, d)))
+    q = bits(g.standard_normal((int(new.sum()), hq, d)))
+    cu_q, cu_k = wl.cu_seqlens(new), wl.cu_seqlens(lk)
+    out = oracle.attention_paged_prefill(q, kc, vc, bt, cu_q, cu_k, d ** -0.5)
+    # contiguous reference: walk each sequence's blocks in logical order
+    ks, vs = [], []
+    for b in range(B):
+        for j in range(int(lk[b])):
+            ks.append(kc[bt[b, j // bs], j % bs])
+            vs.append(vc[bt[b, j // bs], j % bs])
+    ref = oracle.attention_varlen(q, np.stack(ks), np.stack(vs), cu_q, cu_k, d ** -0.5, True)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_paged_prefill_single_query_is_paged_decode_and_prefix_mean():
+    g = np.random.default_rng(44)
+    d, bs, hq, hkv = 8, 4, 4, 2
+    lk = np.array([6, 9])
+    nb = 6
+    bt = wl.carve_block_tables(g.permutation(nb).astype(np.int32), lk, block_size=bs)
+    kc = bits(g.standard_normal((nb, bs, hkv, d)))
+    vc = bits(g.standard_normal((nb, bs, hkv, d)))
+    q = bits(g.standard_normal((2, hq, d)))
+    one = wl.cu_seqlens([1, 1])
+    pre = oracle.attention_paged_prefill(q, kc, vc, bt, one, wl.cu_seqlens(lk), 0.3)
+    dec = oracle.paged_decode(q, kc, vc, bt, lk.astype(np.int32), 0.3)
+    np.testing.assert_allclose(pre, dec, rtol=1e-13, atol=1e-13)
+    # q = 0: query i of a sequence with prefix P averages keys 0 .. P + i
+    q0 = np.zeros((3, hq, d), np.uint16)
+    out = oracle.attention_paged_prefill(q0, kc, vc, bt[:1], wl.cu_seqlens([3]),
+                                         wl.cu_seqlens([6]), 0.3)
+    for i in range(3):
+        rows = [vc[bt[0, j // bs], j % bs] for j in range(3 + i + 1)]
+        mean = F32(np.stack(rows)).astype(np.float64).mean(0)
+        for h in range(hq):
+            np.testing.assert_allclose(out[i, h], mean[h // (hq // hkv)], rtol=1e-12, atol=1e-12)
