@@ -7,6 +7,7 @@
  *   nv_qknorm_rope          per-head RMSNorm of q and k, then RoPE, in place
  *   nv_store_kvcache        scatter new K/V rows into the paged cache
  *   nv_prefill_attn_varlen  causal GQA attention over packed sequences
+ *   nv_prefill_attn_paged   the same with K/V read through the block table
  *   nv_decode_attn_paged    single-query GQA attention over the paged cache
  * plus nv_rope_cos_sin_cache (builds the RoPE table once) and the decode
  * workspace query.
@@ -172,13 +173,16 @@ NV_API int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride,
  *   cu_seqlens_q, cu_seqlens_k   [B + 1] int32, device.
  *   max_seqlen_q, max_seqlen_k   upper bounds of the per-sequence lengths
  *                                (they size the grid; larger is safe).
- * This version requires causal == 1 and equal q and k lengths per
- * sequence (cu_seqlens_q == cu_seqlens_k element-wise; prefill without a
- * cached prefix).  Rows of other sequences that share a 128-row tile are
- * read but masked, so every row of k and v must hold finite values.
+ * Causality is aligned to the last key: with Lq queries and Lk keys in a
+ * sequence, query i sees keys j <= Lk - Lq + i, so equal lengths give the
+ * plain prefill and Lk > Lq a prefill whose first Lk - Lq keys are an
+ * earlier prefix.  Requires causal == 1 and Lk >= Lq for every sequence (a
+ * sequence with Lk < Lq is skipped and counted in err_count).  Rows of other
+ * sequences that share a 128-row tile are read but masked, so every row of
+ * k and v must hold finite values.
  * Requires head_dim == 128, token strides multiples of 8, 16-byte aligned
- * pointers, total_q, total_k < 2^31.  err_count (optional) only records
- * NV_ERR_PIPELINE_FAILURE.
+ * pointers, total_q, total_k < 2^31.  err_count (optional) counts skipped
+ * sequences and records NV_ERR_PIPELINE_FAILURE.
  */
 NV_API int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
                            const nv_bf16_t *k, int64_t k_tok_stride,
@@ -188,6 +192,37 @@ NV_API int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
                            int64_t total_k, int max_seqlen_q, int max_seqlen_k,
                            int Hq, int Hkv, int head_dim, float softmax_scale,
                            int causal, int *err_count, void *stream);
+
+/*
+ * Prefill over the paged cache: a prefix-cache hit, or a later chunk of a
+ * chunked prefill.  "3.3 Model skeleton and core operators", sec. 7.2 (when
+ * K/V of the step already sit in the cache, k and v are replaced by the
+ * whole k_cache / v_cache and block_table is passed; cu_seqlens_k[-1] >
+ * cu_seqlens_q[-1]); "nano-vllm code walkthrough", Prefill stage case 2.
+ * Sequence b has Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b] new queries and
+ * Lk = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys, all already in the cache
+ * (nv_store_kvcache wrote the new ones first); logical key j lives at
+ * k_cache[block_tables[b][j / block_size], j % block_size, h / G].  Query i
+ * sees keys j <= Lk - Lq + i.  Same tcgen05 kernel as
+ * nv_prefill_attn_varlen, with K/V tiles gathered through the block table.
+ *   q             [total_q, Hq, head_dim] bf16, token stride q_tok_stride.
+ *   k_cache, v_cache  [num_blocks, block_size, Hkv, head_dim] bf16.
+ *   block_tables  [B, max_blocks_per_seq] int32.
+ *   o             [total_q, Hq, head_dim] bf16, contiguous, written.
+ * A block id outside [0, num_blocks) is counted in err_count and reads as
+ * zeros; a sequence with Lk < Lq or Lk > max_blocks_per_seq * block_size is
+ * skipped and counted.  Cache rows past Lk may hold any bits.  Requires
+ * head_dim == 128, block_size % 128 == 0, causal == 1, 16-byte aligned
+ * pointers, q_tok_stride a multiple of 8.
+ */
+NV_API int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
+                                 const nv_bf16_t *k_cache, const nv_bf16_t *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 nv_bf16_t *o, const int32_t *cu_seqlens_q,
+                                 const int32_t *cu_seqlens_k, int B, int64_t total_q,
+                                 int max_seqlen_q, int Hq, int Hkv, int head_dim,
+                                 int block_size, int64_t num_blocks, float softmax_scale,
+                                 int causal, int *err_count, void *stream);
 
 /*
  * Bytes of fp32 workspace nv_decode_attn_paged needs for these sizes and

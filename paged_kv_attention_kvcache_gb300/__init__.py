@@ -26,13 +26,13 @@ from .build import LIB_PATH
 __all__ = [
     "NvAttnError", "library", "library_path", "nv_version",
     "nv_rope_cos_sin_cache", "nv_add_rmsnorm", "nv_qknorm_rope", "nv_store_kvcache",
-    "nv_prefill_attn_varlen", "nv_decode_attn_workspace_size", "nv_decode_attn_paged",
-    "ABI_FUNCTIONS",
+    "nv_prefill_attn_varlen", "nv_prefill_attn_paged", "nv_decode_attn_workspace_size",
+    "nv_decode_attn_paged", "ABI_FUNCTIONS",
 ]
 
 ABI_FUNCTIONS = (
     "nv_status_string", "nv_version", "nv_rope_cos_sin_cache", "nv_add_rmsnorm",
-    "nv_qknorm_rope", "nv_store_kvcache", "nv_prefill_attn_varlen",
+    "nv_qknorm_rope", "nv_store_kvcache", "nv_prefill_attn_varlen", "nv_prefill_attn_paged",
     "nv_decode_attn_workspace_size", "nv_decode_attn_paged", "nv_decode_attn_paged_noalloc",
 )
 
@@ -48,6 +48,8 @@ _SIGNATURES = {
     "nv_store_kvcache": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I64, _P, _P], _I32),
     "nv_prefill_attn_varlen": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I32,
                                 _I32, _I32, _I32, _I32, _F32, _I32, _P, _P], _I32),
+    "nv_prefill_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _I64, _I32, _I32, _I32,
+                               _I32, _I32, _I64, _F32, _I32, _P, _P], _I32),
     "nv_decode_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "nv_decode_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32,
                               _I64, _F32, _I32, _P, _SZ, _P, _P], _I32),
@@ -174,6 +176,23 @@ def nv_prefill_attn_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q:
         _ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(o), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
         B, Tq, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), Hq, k.shape[1], d,
         float(softmax_scale), 1 if causal else 0, _ptr(err_count), _stream(stream)))
+
+
+def nv_prefill_attn_paged(q, k_cache, v_cache, block_tables, o, cu_seqlens_q, cu_seqlens_k,
+                          max_seqlen_q: int, softmax_scale: float, causal: bool = True,
+                          err_count=None, stream=None) -> None:
+    """Prefill whose keys (cached prefix + new tokens) are read from the paged
+    cache through block_tables; o [Tq, Hq, 128] contiguous is written."""
+    qs = _heads_view(q, "q")
+    if not o.is_contiguous() or not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("o and the caches must be contiguous")
+    Tq, Hq, d = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    B = cu_seqlens_q.shape[0] - 1
+    _check("nv_prefill_attn_paged", library().nv_prefill_attn_paged(
+        _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(o), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Tq, int(max_seqlen_q), Hq, Hkv, d,
+        bs, nb, float(softmax_scale), 1 if causal else 0, _ptr(err_count), _stream(stream)))
 
 
 def nv_decode_attn_workspace_size(B, Hq, Hkv, head_dim, max_blocks_per_seq, block_size,

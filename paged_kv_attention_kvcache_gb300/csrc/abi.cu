@@ -201,7 +201,67 @@ int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf
     p.max_seqlen_q = max_seqlen_q;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.err_count = err_count;
-    return launch_status(launch_prefill(p, q_map, k_map, v_map, as_stream(stream)));
+    p.block_tables = nullptr;
+    p.max_blocks = 0;
+    p.block_size = 0;
+    p.num_blocks = 0;
+    return launch_status(launch_prefill(p, q_map, k_map, v_map, false, as_stream(stream)));
+}
+
+int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf16_t *k_cache,
+                          const nv_bf16_t *v_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, nv_bf16_t *o, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, int B, int64_t total_q, int max_seqlen_q,
+                          int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
+                          float softmax_scale, int causal, int *err_count, void *stream) {
+    if (B < 0 || total_q < 0 || max_seqlen_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
+        max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        !(softmax_scale > 0.f) || !isfinite(softmax_scale))
+        return NV_EINVAL;
+    if (head_dim != 128 || causal != 1 || block_size % 128 != 0) return NV_EUNSUPPORTED;
+    if (total_q >= 0x7FFFFFFF || B > 65535 || Hq > 65535 || num_blocks > 0x7FFFFFFF ||
+        (int64_t)max_blocks_per_seq * block_size > 0x7FFFFFFF)
+        return NV_EUNSUPPORTED;
+    if (B == 0 || total_q == 0 || max_seqlen_q == 0) return NV_OK;
+    if (!q || !k_cache || !v_cache || !o || !block_tables || !cu_seqlens_q || !cu_seqlens_k)
+        return NV_EINVAL;
+    if (q_tok_stride < (int64_t)Hq * 128) return NV_EINVAL;
+    if (q_tok_stride % 8 || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(o))
+        return NV_EALIGN;
+    if ((int64_t)(max_seqlen_q + 127) / 128 > 65535) return NV_EUNSUPPORTED;
+
+    CUtensorMap q_map, k_map, v_map;
+    {
+        const uint64_t dims[3] = {128, (uint64_t)Hq, (uint64_t)total_q};
+        const uint64_t strides[2] = {128 * 2, (uint64_t)q_tok_stride * 2};
+        const uint32_t box[3] = {64, 1, 128};
+        if (!make_tensor_map_bf16(&q_map, q, 3, dims, strides, box)) return NV_EDRIVER;
+    }
+    {
+        const uint64_t dims[4] = {128, (uint64_t)Hkv, (uint64_t)block_size, (uint64_t)num_blocks};
+        const uint64_t strides[3] = {128 * 2, (uint64_t)Hkv * 128 * 2,
+                                     (uint64_t)block_size * Hkv * 128 * 2};
+        const uint32_t box[4] = {64, 1, 128, 1};
+        if (!make_tensor_map_bf16(&k_map, k_cache, 4, dims, strides, box) ||
+            !make_tensor_map_bf16(&v_map, v_cache, 4, dims, strides, box))
+            return NV_EDRIVER;
+    }
+    PrefillParams p;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.cu_seqlens_k = cu_seqlens_k;
+    p.o = o;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.max_seqlen_q = max_seqlen_q;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.err_count = err_count;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks_per_seq;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    return launch_status(launch_prefill(p, q_map, k_map, v_map, true, as_stream(stream)));
 }
 
 size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim,

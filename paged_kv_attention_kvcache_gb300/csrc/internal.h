@@ -63,10 +63,17 @@ struct PrefillParams {
     int max_seqlen_q;
     float scale_log2;
     int *err_count;
+    // Paged K/V only: keys come from the cache through the block table.
+    const int32_t *block_tables;
+    int max_blocks;
+    int block_size;            // multiple of 128
+    int64_t num_blocks;
 };
 
+// paged == false: k/v maps are 3-D [128, Hkv, total_k] over contiguous k/v;
+// paged == true: 4-D [128, Hkv, block_size, num_blocks] over the caches.
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
-                           const CUtensorMap &k_map, const CUtensorMap &v_map,
+                           const CUtensorMap &k_map, const CUtensorMap &v_map, bool paged,
                            cudaStream_t s);
 
 // --------------------------------------------------------------------- TMA

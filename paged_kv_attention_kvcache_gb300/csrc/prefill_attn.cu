@@ -72,13 +72,20 @@ struct Barriers {
 // One unit of work: a pair of 128-row query tiles of one head of one
 // sequence.  Items are numbered heaviest first (pair index descending, then
 // sequence, then head, so the heads sharing a kv head are adjacent).
+// A sequence has Lq queries and Lk >= Lq keys; query i sits at key position
+// off + i with off = Lk - Lq (causality aligned to the last key: off = 0 for
+// a plain prefill, the cached prefix length for a prefix hit or a chunk).
 struct Item {
-    int h, q_start, L, k_start, q0, kvh;
+    int h, b, q_start, L, Lk, off, k_start, q0, kvh;
     int last[kQTiles];      // last key tile of query tile a (-1: tile has no rows)
+    int mask_from[kQTiles]; // first key tile that can hold keys after some row
     int n_kv;               // key tiles the pair needs
 };
 
-__device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n_pairs, Item &it) {
+// Returns false for an item with no rows; *bad is set when the sequence is
+// malformed (Lk < Lq), in which case no role touches it.
+__device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n_pairs, Item &it,
+                                            bool *bad = nullptr) {
     const int h = w % p.Hq;
     const int t = w / p.Hq;
     const int b = t % p.B;
@@ -87,19 +94,40 @@ __device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n
     const int L = __ldg(p.cu_seqlens_q + b + 1) - q_start;
     const int q0 = pair * kQTiles * kBM;
     if (q0 >= L) return false;
-    const int qt0 = pair * kQTiles;
-    const bool has1 = q0 + kBM < L;
+    const int k_start = __ldg(p.cu_seqlens_k + b);
+    int Lk = __ldg(p.cu_seqlens_k + b + 1) - k_start;
+    if (p.block_tables && Lk > p.max_blocks * p.block_size) Lk = -1;   // beyond the table
+    if (Lk < L) {
+        if (bad) *bad = true;
+        return false;
+    }
+    const int off = Lk - L;
+    const int nk = (Lk + kBN - 1) / kBN;
     it.h = h;
+    it.b = b;
     it.q_start = q_start;
     it.L = L;
-    it.k_start = __ldg(p.cu_seqlens_k + b);
+    it.Lk = Lk;
+    it.off = off;
+    it.k_start = k_start;
     it.q0 = q0;
     it.kvh = h / (p.Hq / p.Hkv);
-    it.last[0] = qt0;
-    it.last[1] = has1 ? qt0 + 1 : -1;
-    it.n_kv = has1 ? qt0 + 2 : qt0 + 1;
+    it.n_kv = 0;
+    for (int a = 0; a < kQTiles; ++a) {
+        const int qa = q0 + a * kBM;
+        if (qa >= L) {
+            it.last[a] = -1;
+            it.mask_from[a] = 0;
+            continue;
+        }
+        const int lt = (off + qa + kBM - 1) / kBN;
+        it.last[a] = lt < nk - 1 ? lt : nk - 1;
+        it.mask_from[a] = (off + qa) / kBN;
+        if (it.last[a] + 1 > it.n_kv) it.n_kv = it.last[a] + 1;
+    }
     return true;
 }
+
 constexpr int kPrefillSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
 
 // ------------------------------------------------------------ tcgen05 PTX
@@ -225,6 +253,10 @@ __device__ __forceinline__ void record_failure(Barriers *bars, int *err_count) {
 
 }  // namespace
 
+// kPaged: K/V tiles come from the paged cache through the block table.
+// kOffset: some sequence may have Lk > Lq (causality aligned to the last key);
+// without it every sequence has Lk == Lq and only diagonal tiles mask.
+template <bool kPaged, bool kOffset>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
 prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap k_map,
@@ -280,15 +312,33 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             // K runs one tile ahead of V, so QK^T of the next tile never waits
             // behind PV; the next item's Q and first K load while the current
             // item drains.
+            // One 128-key tile: contiguous rows k_start + 128 j, or (paged) the
+            // 128-token half of block block_tables[b][128 j / block_size].  A
+            // block id outside the pool is counted and loads zeros (a TMA
+            // coordinate outside the tensor fills zeros).
+            auto load_tile = [&](const CUtensorMap *map, uint8_t *dst, uint64_t *bar,
+                                 const Item &it, int j) {
+                if (kPaged) {
+                    const int key = j * kBN;
+                    int blk = __ldg(p.block_tables + (int64_t)it.b * p.max_blocks + key / p.block_size);
+                    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                        count_error(p.err_count);
+                        blk = -1;
+                    }
+                    tma_load_4d(dst, map, bar, 0, it.kvh, key % p.block_size, blk);
+                    tma_load_4d(dst + kHalf, map, bar, 64, it.kvh, key % p.block_size, blk);
+                } else {
+                    tma_load_3d(dst, map, bar, 0, it.kvh, it.k_start + j * kBN);
+                    tma_load_3d(dst + kHalf, map, bar, 64, it.kvh, it.k_start + j * kBN);
+                }
+            };
             auto load_k = [&](const Item &it, int j) {
                 const int st = kcnt % kKStages;
                 if (kcnt >= kKStages &&
                     !mbar_wait(&bars->k_empty[st], ((kcnt / kKStages) - 1) & 1))
                     return false;
-                uint8_t *sK = smem + kOffK + st * kTileBytes;
                 mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-                tma_load_3d(sK, &k_map, &bars->k_full[st], 0, it.kvh, it.k_start + j * kBN);
-                tma_load_3d(sK + kHalf, &k_map, &bars->k_full[st], 64, it.kvh, it.k_start + j * kBN);
+                load_tile(&k_map, smem + kOffK + st * kTileBytes, &bars->k_full[st], it, j);
                 ++kcnt;
                 return true;
             };
@@ -297,16 +347,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (vcnt >= kVStages &&
                     !mbar_wait(&bars->v_empty[st], ((vcnt / kVStages) - 1) & 1))
                     return false;
-                uint8_t *sV = smem + kOffV + st * kTileBytes;
                 mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                tma_load_3d(sV, &v_map, &bars->v_full[st], 0, it.kvh, it.k_start + j * kBN);
-                tma_load_3d(sV + kHalf, &v_map, &bars->v_full[st], 64, it.kvh, it.k_start + j * kBN);
+                load_tile(&v_map, smem + kOffV + st * kTileBytes, &bars->v_full[st], it, j);
                 ++vcnt;
                 return true;
             };
             for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
                 Item it;
-                if (!decode_item(w, p, n_pairs, it)) continue;
+                bool bad = false;
+                if (!decode_item(w, p, n_pairs, it, &bad)) {
+                    if (bad) count_error(p.err_count);
+                    continue;
+                }
                 const bool has1 = it.last[1] >= 0;
                 if (qcnt >= 1 && !mbar_wait(&bars->q_empty, (qcnt - 1) & 1)) {
                     ok = false;
@@ -349,6 +401,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             ++qcnt;
             // Key tile j of this item is ring slot kbase + j (same for V).
             const int kbase = kcnt, vbase = vcnt;
+            // Paged: first row past Lk in the item's last key tile (-1: none).
+            const int tail = it.Lk - (it.n_kv - 1) * kBN;
+            const int zero_from = (kPaged && tail < kBN) ? tail : -1;
+            bool tail_cleared = false;
             int k_ready = -1, v_ready = -1;
             int s_left = (it.last[0] + 1) + (has1 ? it.last[1] + 1 : 0);
             auto ensure_k = [&](int j) {
@@ -395,6 +451,20 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (j + 1 <= it.last[a]) ensure_k(j + 1);
                 if (ok && j == 0 && ocnt[a] >= 1)     // epilogue of the previous item done
                     ok = wait_all(&bars->o_empty[a], (ocnt[a] - 1) & 1);
+                if (kPaged && ok && zero_from >= 0 && j == it.n_kv - 1 && !tail_cleared) {
+                    tail_cleared = true;
+                    // Cache rows past Lk in the last tile may hold any bits;
+                    // their probability is zero but 0 * NaN is not, so clear
+                    // them before the first PV reads the tile.
+                    uint8_t *sV = smem + kOffV + ((vbase + j) % kVStages) * kTileBytes;
+                    for (int idx = zero_from * 8 + lane; idx < kBN * 8; idx += 32) {
+                        const int r = idx >> 3, c = idx & 7;
+                        *reinterpret_cast<uint4 *>(sV + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(sV + kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 if (ok) ok = wait_all(&bars->p_full[a], pcnt[a] & 1);
                 if (!ok) return;
                 ++pcnt[a];
@@ -444,8 +514,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
             Item it;
             if (!decode_item(w, p, n_pairs, it)) continue;
-            const int last = it.last[a];
+            const int last = a ? it.last[1] : it.last[0];
             if (last < 0) continue;                       // this query tile has no rows
+            // kOffset: keys after a row can reach into tile mask_from = last - 1;
+            // row `row` sees key c of tile j iff c <= vis_row - 128 j.  Without
+            // it (Lk == Lq) only the diagonal tile masks, at c <= row.
+            const int mask_from = kOffset ? (a ? it.mask_from[1] : it.mask_from[0]) : last;
+            const int vis_row = kOffset ? it.off + it.q0 + a * kBM + row : 0;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; ok && j <= last; ++j) {
                 if (!mbar_wait(&bars->s_full[a], scnt & 1)) {
@@ -455,11 +530,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 ++scnt;
                 tc_fence_after();
                 // Pass 1: row max over the 128 scores, 32 columns at a time.  Only
-                // the diagonal tile masks (key c > row); the others pay nothing.
-                const bool diag = j == last;
-                float mx8[8];
+                // tiles that can hold keys after some row mask (key c visible
+                // iff c <= vis); the others pay nothing.
+                const bool diag = kOffset ? j >= mask_from : j == last;
+                const int vis = kOffset ? vis_row - j * kBN : row;
+                float mx4[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+                for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
                 if (!diag) {
                     // The next chunk's load is in flight while this one is reduced.
                     uint32_t rb[2][32];
@@ -471,7 +548,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         const uint32_t (&r)[32] = rb[c & 1];
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            mx8[e & 7] = fmax3(mx8[e & 7], __uint_as_float(r[2 * e]),
+                            mx4[e & 3] = fmax3(mx4[e & 3], __uint_as_float(r[2 * e]),
                                                __uint_as_float(r[2 * e + 1]));
                         if (c < 3) tmem_wait_ld();
                     }
@@ -483,11 +560,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (c * 32 + e <= row) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(r[e]));
+                            if (c * 32 + e <= vis) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(r[e]));
                     }
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
                 const float m_new = fmaxf(m_used, mx * sl2);
                 float alpha = 1.f;
                 const bool rescale = m_new > m_used + kRescaleThreshold;
@@ -547,8 +623,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int k0 = c * 32 + 2 * e;
-                            const float p0 = k0 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
-                            const float p1 = k0 + 1 <= row ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
+                            const float p0 = k0 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
+                            const float p1 = k0 + 1 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
                             sum4[e & 3] += p0 + p1;
                             pk[e] = pack_bf16x2(p0, p1);
                         }
@@ -606,12 +682,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     }
 }
 
-cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
-                           const CUtensorMap &k_map, const CUtensorMap &v_map,
-                           cudaStream_t s) {
+template <bool kPaged, bool kOffset>
+static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q_map,
+                                    const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                    cudaStream_t s) {
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel,
+        cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<kPaged, kOffset>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kPrefillSmemBytes);
         if (e != cudaSuccess) return e;
@@ -626,9 +703,19 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
         sms = 148;
     // Persistent: one CTA per SM, each walking items blockIdx.x, +grid, ...
     const int grid = (int)(items < sms ? items : sms);
-    prefill_attn_kernel<<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(q_map, k_map, v_map, p,
-                                                                         n_pairs, (int)items);
+    prefill_attn_kernel<kPaged, kOffset><<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(
+        q_map, k_map, v_map, p, n_pairs, (int)items);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
+                           const CUtensorMap &k_map, const CUtensorMap &v_map, bool paged,
+                           cudaStream_t s) {
+    if (paged) return launch_prefill_t<true, true>(p, q_map, k_map, v_map, s);
+    // One cu_seqlens array for queries and keys proves Lk == Lq everywhere.
+    if (p.cu_seqlens_k == p.cu_seqlens_q)
+        return launch_prefill_t<false, false>(p, q_map, k_map, v_map, s);
+    return launch_prefill_t<false, true>(p, q_map, k_map, v_map, s);
 }
 
 }  // namespace nvattn

@@ -143,3 +143,19 @@ def test_rope_table_rejects_bad_arguments(lib):
     assert f(FAKE, 16, 128, 0.5, None) == NV_EINVAL
     assert f(None, 16, 128, 1e6, None) == NV_EINVAL
     assert f(None, 0, 128, 1e6, None) == NV_OK
+
+
+def test_paged_prefill_rejects_bad_arguments(lib):
+    f = lib.nv_prefill_attn_paged
+
+    def call(bs=256, d=128, causal=1, bt=FAKE, q=FAKE, Hq=32, Hkv=8, B=2):
+        return f(q, 4096, FAKE, FAKE, bt, 16, FAKE, FAKE, FAKE, B, 100, 64, Hq, Hkv, d, bs, 1000,
+                 0.088, causal, None, None)
+
+    assert call(bs=192) == NV_EUNSUPPORTED          # block must hold whole 128-key tiles
+    assert call(d=64) == NV_EUNSUPPORTED
+    assert call(causal=0) == NV_EUNSUPPORTED
+    assert call(bt=None) == NV_EINVAL
+    assert call(Hq=12) == NV_EINVAL
+    assert call(q=MIS) == NV_EALIGN
+    assert call(B=0) == NV_OK

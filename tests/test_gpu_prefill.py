@@ -2,6 +2,8 @@
 The first case launches a single CTA; later ones span several 128-row tiles
 with ragged tails, GQA groups, strided q/k/v views and the full Qwen3-8B
 batch (sampled rows)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -91,3 +93,82 @@ def test_prefill_qwen3_8b_batch_full_size_sampled():
     q, k, v = split_qkv(batch.qkv, s.hq, s.hkv)
     ref = oracle.attention_varlen(q, k, v, cu, cu, SCALE, True, rows=rows)
     check_close(got[rows[:, 0], rows[:, 1]], ref, "prefill cfg4 sampled")
+
+
+# ------------------------------------------- keys beyond the queries (prefix)
+def test_prefill_contiguous_keys_with_prefix():
+    # Each sequence's keys are a prefix followed by its Lq new tokens; query i
+    # sees keys <= Lk - Lq + i (causality aligned to the last key).
+    hq, hkv = 8, 2
+    new = np.array([5, 130, 1, 257])
+    prefix = np.array([0, 100, 300, 129])
+    lk = new + prefix
+    g = np.random.default_rng(530)
+    q = wl.f32_to_bf16_bits(g.standard_normal((int(new.sum()), hq, 128)).astype(np.float32))
+    k = wl.f32_to_bf16_bits(g.standard_normal((int(lk.sum()), hkv, 128)).astype(np.float32))
+    v = wl.f32_to_bf16_bits(g.standard_normal((int(lk.sum()), hkv, 128)).astype(np.float32))
+    cu_q, cu_k = wl.cu_seqlens(new), wl.cu_seqlens(lk)
+    o = torch.empty(int(new.sum()), hq, 128, dtype=torch.bfloat16, device="cuda")
+    err = err_counter()
+    nv.nv_prefill_attn_varlen(dev(q), dev(k), dev(v), o, dev_i32(cu_q), dev_i32(cu_k),
+                              int(new.max()), int(lk.max()), SCALE, err_count=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.attention_varlen(q, k, v, cu_q, cu_k, SCALE, True)
+    check_close(host(o), ref, "prefill with contiguous prefix")
+
+
+def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3):
+    g = np.random.default_rng(seed)
+    prefix, new = np.asarray(prefix), np.asarray(new)
+    lk = prefix + new
+    bs = wl.BLOCK_SIZE
+    nb = int(sum(math.ceil(int(x) / bs) for x in lk)) + spare
+    bt = wl.carve_block_tables(g.permutation(nb).astype(np.int32), lk)
+    kc = wl.f32_to_bf16_bits(g.standard_normal((nb, bs, hkv, 128)).astype(np.float32))
+    vc = wl.f32_to_bf16_bits(g.standard_normal((nb, bs, hkv, 128)).astype(np.float32))
+    if nan_tail:
+        # rows past each sequence's last key hold NaN bits
+        for b, L in enumerate(lk):
+            last = bt[b, (int(L) - 1) // bs]
+            kc[last, int(L) % bs if L % bs else bs:] = 0x7FC0
+            vc[last, int(L) % bs if L % bs else bs:] = 0x7FC0
+    q = wl.f32_to_bf16_bits(g.standard_normal((int(new.sum()), hq, 128)).astype(np.float32))
+    cu_q, cu_k = wl.cu_seqlens(new), wl.cu_seqlens(lk)
+    o = torch.empty(int(new.sum()), hq, 128, dtype=torch.bfloat16, device="cuda")
+    err = err_counter()
+    nv.nv_prefill_attn_paged(dev(q), dev(kc), dev(vc), dev_i32(bt), o, dev_i32(cu_q),
+                             dev_i32(cu_k), int(new.max()), SCALE, err_count=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.attention_paged_prefill(q, kc, vc, bt, cu_q, cu_k, SCALE, rows=rows)
+    got = host(o)
+    if rows is not None:
+        got = got[rows[:, 0], rows[:, 1]]
+    return got, ref
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2), (32, 8)])
+def test_prefill_paged_prefix_hit(hq, hkv):
+    got, ref = _paged_case(540 + hq, prefix=[0, 37, 256, 300, 511, 1000],
+                           new=[5, 1, 128, 200, 129, 300], hq=hq, hkv=hkv)
+    check_close(got, ref, f"paged prefill {hq}/{hkv}")
+
+
+def test_prefill_paged_equals_contiguous_when_no_prefix():
+    # With no cached prefix the paged path must agree with the contiguous one.
+    got, ref = _paged_case(550, prefix=[0, 0, 0], new=[37, 300, 128], hq=16, hkv=8)
+    check_close(got, ref, "paged prefill, no prefix")
+
+
+def test_prefill_paged_chunked_qwen3_8b_sampled():
+    # Chunked prefill at Qwen3-8B heads: 8 sequences with U[0, 4096] cached
+    # tokens and a U[128, 1024] chunk each.
+    g = np.random.default_rng(560)
+    prefix = g.integers(0, 4096, 8, endpoint=True)
+    new = g.integers(128, 1024, 8, endpoint=True)
+    cu = wl.cu_seqlens(new)
+    toks = np.concatenate([cu[:-1], cu[1:] - 1, g.integers(0, int(new.sum()), 300)])
+    rows = np.stack([toks, g.integers(0, 32, toks.size)], axis=1).astype(np.int64)
+    got, ref = _paged_case(561, prefix, new, 32, 8, rows=rows)
+    check_close(got, ref, "chunked prefill 8b")
