@@ -336,13 +336,90 @@ def run_ours(args, rank, world, local_rank):
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_val = world * nbytes["total"] / (statistics.mean(e2e_ms) / 1e3) / 1e9
 
+    graph_info = graph_decode_overhead(dev_t)
+
     return dict(
+        graph=graph_info,
         value=value, ms_per_step=tot_ms / args.steps, dec_ms=statistics.mean(dec_ms),
         pre_ms=statistics.mean(pre_ms), attn_ms=statistics.mean(attn_ms),
         attn_gbs=attn_gbs, ptflops=ptflops, pattn_ms=pattn_sum / args.steps, clocks=clk,
         hbm=hbm, bf16=bf16, bf16_sus=bf16_sus, peak_src=peak_src, nbytes=nbytes,
         launches=launches_per_step * args.steps, e2e=e2e_val, h2d=h2d, d2h=d2h, wall=wall,
         gen_s=gen_s, step=step, pre=pre, ws_bytes=ws_bytes, T=T)
+
+
+# ------------------------------------------ launch overhead: CUDA graph
+def graph_decode_overhead(dev_t, reps: int = 200):
+    """A small decode layer step (Qwen3-8B heads, bucket of 8 rows, 6 real
+    sequences of ~2k keys, 2 padded rows with slot -1 and ctx 0): the four
+    ABI calls timed eagerly and as one captured CUDA graph replay."""
+    import torch
+    import paged_kv_attention_kvcache_gb300 as nv
+    s = wl.QWEN3_8B
+    bucket, n_real = 8, 6
+    ctx = np.zeros(bucket, np.int32)
+    ctx[:n_real] = 2048
+    step = wl.make_decode(77, s, np.maximum(ctx, 1), 8 * 8 + 2, with_norms=True, name="graph")
+    step.context_lens[:] = ctx
+    step.slot_mapping[n_real:] = -1
+    Q, D = s.q_size, s.kv_size
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).to(dev_t)
+
+    table = torch.empty(wl.MAX_POSITION, 128, dtype=torch.float32, device=dev_t)
+    nv.nv_rope_cos_sin_cache(table, wl.ROPE_BASE)
+    kc, vc = dev(step.pool.k), dev(step.pool.v)
+    x, r, g = dev(step.x), dev(step.residual), dev(step.gamma)
+    y = torch.empty_like(x)
+    qkv = dev(step.qkv)
+    qn, kn = dev(step.q_norm_w), dev(step.k_norm_w)
+    pos = torch.from_numpy(step.positions).to(dev_t)
+    slots = torch.from_numpy(step.slot_mapping).to(dev_t)
+    bt = torch.from_numpy(step.block_tables).to(dev_t)
+    cl = torch.from_numpy(step.context_lens).to(dev_t)
+    o = torch.empty(bucket, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
+    wsb = nv.nv_decode_attn_workspace_size(bucket, s.hq, s.hkv, 128, bt.shape[1], 256, 0)
+    ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
+    q = qkv[:, :Q].view(bucket, s.hq, 128)
+    k = qkv[:, Q:Q + D].view(bucket, s.hkv, 128)
+    v = qkv[:, Q + D:].view(bucket, s.hkv, 128)
+
+    def layer():
+        nv.nv_add_rmsnorm(x, r, g, y, r, eps=wl.RMS_EPS)
+        nv.nv_qknorm_rope(q, k, qn, kn, table, pos, eps=wl.RMS_EPS)
+        nv.nv_store_kvcache(k, v, kc, vc, slots)
+        nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws)
+
+    side = torch.cuda.Stream(device=dev_t)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            layer()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer()
+
+    def timed(fn):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    eager_us = timed(layer)
+    graph_us = timed(graph.replay)
+    return {"batch_bucket": bucket, "real_sequences": n_real, "ctx": 2048,
+            "eager_us_per_step": eager_us, "graph_us_per_step": graph_us,
+            "kernels_per_step": 4 + (1 if wsb else 0)}
 
 
 # ------------------------------------------------------------ oracle side
@@ -522,6 +599,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": r["e2e"], "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]},
+            "decode_graph": r["graph"],
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
