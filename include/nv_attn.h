@@ -6,6 +6,7 @@
  *   nv_add_rmsnorm          fused residual add + RMSNorm (input_layernorm)
  *   nv_qknorm_rope          per-head RMSNorm of q and k, then RoPE, in place
  *   nv_store_kvcache        scatter new K/V rows into the paged cache
+ *   nv_qknorm_rope_store    the two above in one pass (k goes straight to its slot)
  *   nv_prefill_attn_varlen  causal GQA attention over packed sequences
  *   nv_prefill_attn_paged   the same with K/V read through the block table
  *   nv_decode_attn_paged    single-query GQA attention over the paged cache
@@ -155,6 +156,41 @@ NV_API int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride,
                      const int32_t *slot_mapping, int64_t N, int Hkv,
                      int head_dim, int64_t num_slots, int *err_count,
                      void *stream);
+
+/*
+ * QK-Norm + RoPE + store_kvcache in one pass.  "Nano-vLLM 源码解读 第17篇",
+ * sec. 4 and 5.1, and "3.3 Model skeleton and core operators", sec. 7.1 and
+ * 8: the attention forward rotates q and k and then scatters k and v into
+ * the paged cache; this call does both steps per token, so the rotated k
+ * goes from registers straight to its cache slot.  For in-range positions
+ * the result is exactly that of nv_qknorm_rope followed by
+ * nv_store_kvcache on the same arguments, bit for bit, except that k in
+ * place is written only when
+ * write_k == 1 (the contiguous prefill reads it there; decode and the
+ * paged prefill read the cache and pass write_k == 0).
+ *   q, k, v      [T, Hq|Hkv|Hkv, head_dim] bf16 views, token strides as given;
+ *                q is rotated in place, v is only read.
+ *   q_norm_weight, k_norm_weight, cos_sin, positions, eps   as nv_qknorm_rope.
+ *   slot_mapping [T] int32; -1 = padding (nothing cached for that token).
+ *   k_cache, v_cache [num_blocks, block_size, Hkv, head_dim] bf16,
+ *                num_slots = num_blocks * block_size.
+ * A slot outside [0, num_slots) other than -1 is counted once per token and
+ * the token's rows are not cached; a position outside [0, max_position) is
+ * counted per q and k row as in nv_qknorm_rope, and leaves q, k and the
+ * token's k cache row untouched (its v row is still copied).  Requires
+ * head_dim == 128, token strides multiples of 8, 16-byte aligned pointers.
+ * T == 0 is a no-op.  No counterpart in nano-vllm, which runs the two steps
+ * as separate kernels; it is a design variant of the same step order.
+ */
+NV_API int nv_qknorm_rope_store(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
+                                int64_t k_tok_stride, const nv_bf16_t *v,
+                                int64_t v_tok_stride, const nv_bf16_t *q_norm_weight,
+                                const nv_bf16_t *k_norm_weight, const float *cos_sin,
+                                int max_position, const int64_t *positions,
+                                const int32_t *slot_mapping, nv_bf16_t *k_cache,
+                                nv_bf16_t *v_cache, int64_t num_slots, int64_t T, int Hq,
+                                int Hkv, int head_dim, float eps, int write_k,
+                                int *err_count, void *stream);
 
 /*
  * Varlen causal prefill attention.  "3.3 Model skeleton and core

@@ -26,14 +26,14 @@ from .build import LIB_PATH
 __all__ = [
     "NvAttnError", "library", "library_path", "nv_version",
     "nv_rope_cos_sin_cache", "nv_add_rmsnorm", "nv_qknorm_rope", "nv_store_kvcache",
-    "nv_prefill_attn_varlen", "nv_prefill_attn_paged", "nv_decode_attn_workspace_size",
+    "nv_qknorm_rope_store", "nv_prefill_attn_varlen", "nv_prefill_attn_paged", "nv_decode_attn_workspace_size",
     "nv_decode_attn_paged", "ABI_FUNCTIONS",
 ]
 
 ABI_FUNCTIONS = (
     "nv_status_string", "nv_version", "nv_rope_cos_sin_cache", "nv_add_rmsnorm",
-    "nv_qknorm_rope", "nv_store_kvcache", "nv_prefill_attn_varlen", "nv_prefill_attn_paged",
-    "nv_decode_attn_workspace_size", "nv_decode_attn_paged", "nv_decode_attn_paged_noalloc",
+    "nv_qknorm_rope", "nv_store_kvcache", "nv_qknorm_rope_store", "nv_prefill_attn_varlen",
+    "nv_prefill_attn_paged", "nv_decode_attn_workspace_size", "nv_decode_attn_paged", "nv_decode_attn_paged_noalloc",
 )
 
 _P, _I64, _I32, _F32, _F64, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -46,6 +46,8 @@ _SIGNATURES = {
     "nv_qknorm_rope": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I64, _I32, _I32, _I32, _F32,
                         _P, _P], _I32),
     "nv_store_kvcache": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I64, _P, _P], _I32),
+    "nv_qknorm_rope_store": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _I64,
+                              _I64, _I32, _I32, _I32, _F32, _I32, _P, _P], _I32),
     "nv_prefill_attn_varlen": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I32,
                                 _I32, _I32, _I32, _I32, _F32, _I32, _P, _P], _I32),
     "nv_prefill_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _I64, _I32, _I32, _I32,
@@ -159,6 +161,25 @@ def nv_store_kvcache(key, value, k_cache, v_cache, slot_mapping, err_count=None,
     _check("nv_store_kvcache", library().nv_store_kvcache(
         _ptr(key), ks, _ptr(value), vs, _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N,
         Hkv, d, num_slots, _ptr(err_count), _stream(stream)))
+
+
+def nv_qknorm_rope_store(q, k, v, q_norm_weight, k_norm_weight, cos_sin, positions,
+                         k_cache, v_cache, slot_mapping, eps: float = 1e-6, write_k: bool = False,
+                         err_count=None, stream=None) -> None:
+    """QK-Norm + RoPE of q (in place) and k, with k and v written to their
+    cache slots in the same pass; k in place too when write_k is set."""
+    qs = _heads_view(q, "q")
+    ks = _heads_view(k, "k")
+    vs = _heads_view(v, "v")
+    T, Hq, d = q.shape
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    num_slots = k_cache.shape[0] * k_cache.shape[1]
+    _check("nv_qknorm_rope_store", library().nv_qknorm_rope_store(
+        _ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(q_norm_weight), _ptr(k_norm_weight),
+        _ptr(cos_sin), cos_sin.shape[0], _ptr(positions), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), num_slots, T, Hq, k.shape[1], d, float(eps), int(bool(write_k)),
+        _ptr(err_count), _stream(stream)))
 
 
 def nv_prefill_attn_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,

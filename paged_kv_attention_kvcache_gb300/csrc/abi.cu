@@ -155,6 +155,36 @@ int nv_store_kvcache(const nv_bf16_t *key, int64_t key_tok_stride, const nv_bf16
                                               num_slots, err_count, as_stream(stream)));
 }
 
+int nv_qknorm_rope_store(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
+                         int64_t k_tok_stride, const nv_bf16_t *v, int64_t v_tok_stride,
+                         const nv_bf16_t *q_norm_weight, const nv_bf16_t *k_norm_weight,
+                         const float *cos_sin, int max_position, const int64_t *positions,
+                         const int32_t *slot_mapping, nv_bf16_t *k_cache, nv_bf16_t *v_cache,
+                         int64_t num_slots, int64_t T, int Hq, int Hkv, int head_dim, float eps,
+                         int write_k, int *err_count, void *stream) {
+    if (T < 0 || Hq <= 0 || Hkv <= 0 || max_position <= 0 || num_slots < 0 ||
+        !(eps >= 0.f) || !isfinite(eps) || (write_k != 0 && write_k != 1))
+        return NV_EINVAL;
+    if (head_dim != 128) return NV_EUNSUPPORTED;
+    if (T == 0) return NV_OK;
+    if (!q || !k || !v || !q_norm_weight || !k_norm_weight || !cos_sin || !positions ||
+        !slot_mapping || !k_cache || !v_cache)
+        return NV_EINVAL;
+    if (q_tok_stride < (int64_t)Hq * 128 || k_tok_stride < (int64_t)Hkv * 128 ||
+        v_tok_stride < (int64_t)Hkv * 128)
+        return NV_EINVAL;
+    if (q_tok_stride % 8 || k_tok_stride % 8 || v_tok_stride % 8 || !aligned16(q) ||
+        !aligned16(k) || !aligned16(v) || !aligned16(q_norm_weight) ||
+        !aligned16(k_norm_weight) || !aligned16(cos_sin) || !aligned16(k_cache) ||
+        !aligned16(v_cache))
+        return NV_EALIGN;
+    if (T * (int64_t)(Hq + 2 * Hkv) * 8 > (int64_t)0x7FFFFFFF * 256) return NV_EUNSUPPORTED;
+    return launch_status(launch_qknorm_rope_store(
+        q, q_tok_stride, k, k_tok_stride, v, v_tok_stride, q_norm_weight, k_norm_weight, cos_sin,
+        max_position, positions, slot_mapping, k_cache, v_cache, num_slots, T, Hq, Hkv, eps,
+        write_k, err_count, as_stream(stream)));
+}
+
 int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf16_t *k,
                            int64_t k_tok_stride, const nv_bf16_t *v, int64_t v_tok_stride,
                            nv_bf16_t *o, const int32_t *cu_seqlens_q,

@@ -23,6 +23,15 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
                                int max_position, const int64_t *positions, int64_t T, int Hq,
                                int Hkv, float eps, int *err_count, cudaStream_t s);
 
+cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
+                                     int64_t k_stride, const uint16_t *v, int64_t v_stride,
+                                     const uint16_t *qw, const uint16_t *kw,
+                                     const float *cos_sin, int max_position,
+                                     const int64_t *positions, const int32_t *slot_mapping,
+                                     uint16_t *k_cache, uint16_t *v_cache, int64_t num_slots,
+                                     int64_t T, int Hq, int Hkv, float eps, int write_k,
+                                     int *err_count, cudaStream_t s);
+
 cudaError_t launch_store_kvcache(const uint16_t *key, int64_t key_stride, const uint16_t *value,
                                  int64_t value_stride, uint16_t *k_cache, uint16_t *v_cache,
                                  const int32_t *slot_mapping, int64_t N, int D,

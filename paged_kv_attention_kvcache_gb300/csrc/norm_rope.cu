@@ -149,6 +149,65 @@ cudaError_t launch_add_rmsnorm(const uint16_t *x, const uint16_t *residual,
 // its eight pairs and the rotation needs no exchange.  Four rows per warp.
 constexpr int kRopeThreads = 256;
 
+// Normalise and rotate one 128-element head row.  The eight lanes of the
+// group named by `gmask` each hold elements [8j, 8j+8) and [64+8j, 64+8j+8)
+// of `src`; on return out1/out2 hold the lane's rotated elements as packed
+// bf16 pairs.  Shared by the in-place kernel and the fused cache-writing one
+// so that both give the same bits.
+__device__ __forceinline__ void norm_rope_row(const uint16_t *src, const uint16_t *__restrict__ w,
+                                              const float *__restrict__ cs_row, int j,
+                                              unsigned gmask, float eps, uint4 &out1,
+                                              uint4 &out2) {
+    uint4 a = *reinterpret_cast<const uint4 *>(src + 8 * j);
+    uint4 b = *reinterpret_cast<const uint4 *>(src + 64 + 8 * j);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    float x1[8], x2[8];
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x1[2 * e] = bf16_lo(aw[e]);
+        x1[2 * e + 1] = bf16_hi(aw[e]);
+        x2[2 * e] = bf16_lo(bw[e]);
+        x2[2 * e + 1] = bf16_hi(bw[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x1[e], x1[e], fmaf(x2[e], x2[e], ss));
+    ss += __shfl_xor_sync(gmask, ss, 4);
+    ss += __shfl_xor_sync(gmask, ss, 2);
+    ss += __shfl_xor_sync(gmask, ss, 1);
+    const float rstd = rsqrtf(ss * (1.0f / 128.0f) + eps);
+    const uint4 wa = __ldg(reinterpret_cast<const uint4 *>(w + 8 * j));
+    const uint4 wb = __ldg(reinterpret_cast<const uint4 *>(w + 64 + 8 * j));
+    const uint32_t waw[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t wbw[4] = {wb.x, wb.y, wb.z, wb.w};
+    const float4 *cs = reinterpret_cast<const float4 *>(cs_row);
+    const float4 c0 = __ldg(cs + 2 * j), c1 = __ldg(cs + 2 * j + 1);
+    const float4 s0 = __ldg(cs + 16 + 2 * j), s1 = __ldg(cs + 16 + 2 * j + 1);
+    const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float n1[2], n2[2];
+        n1[0] = x1[2 * e] * rstd * bf16_lo(waw[e]);
+        n1[1] = x1[2 * e + 1] * rstd * bf16_hi(waw[e]);
+        n2[0] = x2[2 * e] * rstd * bf16_lo(wbw[e]);
+        n2[1] = x2[2 * e + 1] * rstd * bf16_hi(wbw[e]);
+        float y1[2], y2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float c = cv[2 * e + u], sn = sv[2 * e + u];
+            y1[u] = n1[u] * c - n2[u] * sn;
+            y2[u] = n2[u] * c + n1[u] * sn;
+        }
+        o1[e] = pack_bf16x2(y1[0], y1[1]);
+        o2[e] = pack_bf16x2(y2[0], y2[1]);
+    }
+    out1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    out2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+}
+
 __global__ void __launch_bounds__(kRopeThreads)
 qknorm_rope_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restrict__ k,
                    int64_t k_stride, const uint16_t *__restrict__ qw,
@@ -177,58 +236,13 @@ qknorm_rope_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restr
         if (j == 0) count_error(err_count);
         return;
     }
-    uint4 a = *reinterpret_cast<const uint4 *>(base + 8 * j);
-    uint4 b = *reinterpret_cast<const uint4 *>(base + 64 + 8 * j);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-    float x1[8], x2[8];
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x1[2 * e] = bf16_lo(aw[e]);
-        x1[2 * e + 1] = bf16_hi(aw[e]);
-        x2[2 * e] = bf16_lo(bw[e]);
-        x2[2 * e + 1] = bf16_hi(bw[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x1[e], x1[e], fmaf(x2[e], x2[e], ss));
-    // Reduce over the eight lanes of this row (xor offsets stay inside it).
-    // Groups of the same warp may have returned early, so the shuffle names
-    // only this group's lanes; all eight share the row and its position.
+    // Groups of the same warp may have returned early, so the row's shuffles
+    // name only this group's lanes; all eight share the row and its position.
     const unsigned gmask = 0xFFu << (lane & ~7);
-    ss += __shfl_xor_sync(gmask, ss, 4);
-    ss += __shfl_xor_sync(gmask, ss, 2);
-    ss += __shfl_xor_sync(gmask, ss, 1);
-    const float rstd = rsqrtf(ss * (1.0f / 128.0f) + eps);
-    const uint4 wa = __ldg(reinterpret_cast<const uint4 *>(w + 8 * j));
-    const uint4 wb = __ldg(reinterpret_cast<const uint4 *>(w + 64 + 8 * j));
-    const uint32_t waw[4] = {wa.x, wa.y, wa.z, wa.w};
-    const uint32_t wbw[4] = {wb.x, wb.y, wb.z, wb.w};
-    const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + pos * 128);
-    const float4 c0 = __ldg(cs + 2 * j), c1 = __ldg(cs + 2 * j + 1);
-    const float4 s0 = __ldg(cs + 16 + 2 * j), s1 = __ldg(cs + 16 + 2 * j + 1);
-    const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    uint32_t o1[4], o2[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float n1[2], n2[2];
-        n1[0] = x1[2 * e] * rstd * bf16_lo(waw[e]);
-        n1[1] = x1[2 * e + 1] * rstd * bf16_hi(waw[e]);
-        n2[0] = x2[2 * e] * rstd * bf16_lo(wbw[e]);
-        n2[1] = x2[2 * e + 1] * rstd * bf16_hi(wbw[e]);
-        float y1[2], y2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const float c = cv[2 * e + u], sn = sv[2 * e + u];
-            y1[u] = n1[u] * c - n2[u] * sn;
-            y2[u] = n2[u] * c + n1[u] * sn;
-        }
-        o1[e] = pack_bf16x2(y1[0], y1[1]);
-        o2[e] = pack_bf16x2(y2[0], y2[1]);
-    }
-    *reinterpret_cast<uint4 *>(base + 8 * j) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-    *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+    uint4 o1, o2;
+    norm_rope_row(base, w, cos_sin + pos * 128, j, gmask, eps, o1, o2);
+    *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
+    *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
 }
 
 cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64_t k_stride,
@@ -242,6 +256,92 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
     qknorm_rope_kernel<<<blocks, kRopeThreads, 0, s>>>(q, q_stride, k, k_stride, qw, kw, cos_sin,
                                                        max_position, positions, T, Hq, Hkv, eps,
                                                        err_count);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------ QK-Norm + RoPE + store_kvcache
+// The same per-row arithmetic as qknorm_rope_kernel, with the cache scatter of
+// store_kvcache folded in ("Nano-vLLM 源码解读 第17篇", sec. 4 and 5.1 give
+// the order: rotate q and k, then write k and v to their slots).  A token owns
+// Hq + 2 Hkv rows of 128 elements: q rows are rotated in place, k rows are
+// rotated and written to the token's cache slot (and back in place only when
+// asked), v rows are copied bit for bit to the slot.  Eight lanes per row as
+// above; k never makes the extra round trip through HBM that the separate
+// store kernel would read it back for.
+__global__ void __launch_bounds__(kRopeThreads)
+qknorm_rope_store_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restrict__ k,
+                         int64_t k_stride, const uint16_t *__restrict__ v, int64_t v_stride,
+                         const uint16_t *__restrict__ qw, const uint16_t *__restrict__ kw,
+                         const float *__restrict__ cos_sin, int max_position,
+                         const int64_t *__restrict__ positions,
+                         const int32_t *__restrict__ slot_mapping, uint16_t *__restrict__ k_cache,
+                         uint16_t *__restrict__ v_cache, int64_t num_slots, int64_t T, int Hq,
+                         int Hkv, float eps, int write_k, int *err_count) {
+    const int heads = Hq + 2 * Hkv;
+    const int64_t n_rows = T * heads;
+    const int lane = threadIdx.x & 31;
+    const int j = lane & 7;
+    const int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
+    if (row >= n_rows) return;
+    const int64_t t = row / heads;
+    const int h = (int)(row % heads);
+    const int64_t D = (int64_t)Hkv * 128;
+    int64_t slot = -1;
+    if (h >= Hq) {
+        slot = __ldg(slot_mapping + t);
+        if (slot != -1 && (slot < 0 || slot >= num_slots)) {
+            if (j == 0 && h == Hq) count_error(err_count);   // once per token
+            slot = -1;
+        }
+    }
+    if (h >= Hq + Hkv) {                                        // v: a bit copy
+        if (slot < 0) return;
+        const int hv = h - Hq - Hkv;
+        const uint16_t *src = v + t * v_stride + (int64_t)hv * 128;
+        uint16_t *dst = v_cache + slot * D + (int64_t)hv * 128;
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src + 8 * j));
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 64 + 8 * j));
+        *reinterpret_cast<uint4 *>(dst + 8 * j) = a;
+        *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = b;
+        return;
+    }
+    const bool is_q = h < Hq;
+    uint16_t *base = is_q ? q + t * q_stride + (int64_t)h * 128
+                          : k + t * k_stride + (int64_t)(h - Hq) * 128;
+    const int64_t pos = __ldg(positions + t);
+    if (pos < 0 || pos >= max_position) {
+        if (j == 0) count_error(err_count);
+        return;
+    }
+    const unsigned gmask = 0xFFu << (lane & ~7);
+    uint4 o1, o2;
+    norm_rope_row(base, is_q ? qw : kw, cos_sin + pos * 128, j, gmask, eps, o1, o2);
+    if (is_q || write_k) {
+        *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
+        *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
+    }
+    if (!is_q && slot >= 0) {
+        uint16_t *dst = k_cache + slot * D + (int64_t)(h - Hq) * 128;
+        *reinterpret_cast<uint4 *>(dst + 8 * j) = o1;
+        *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = o2;
+    }
+}
+
+cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
+                                     int64_t k_stride, const uint16_t *v, int64_t v_stride,
+                                     const uint16_t *qw, const uint16_t *kw,
+                                     const float *cos_sin, int max_position,
+                                     const int64_t *positions, const int32_t *slot_mapping,
+                                     uint16_t *k_cache, uint16_t *v_cache, int64_t num_slots,
+                                     int64_t T, int Hq, int Hkv, float eps, int write_k,
+                                     int *err_count, cudaStream_t s) {
+    const int64_t rows = T * (Hq + 2 * Hkv);
+    if (rows == 0) return cudaSuccess;
+    const int64_t threads = rows * 8;
+    const unsigned blocks = (unsigned)((threads + kRopeThreads - 1) / kRopeThreads);
+    qknorm_rope_store_kernel<<<blocks, kRopeThreads, 0, s>>>(
+        q, q_stride, k, k_stride, v, v_stride, qw, kw, cos_sin, max_position, positions,
+        slot_mapping, k_cache, v_cache, num_slots, T, Hq, Hkv, eps, write_k, err_count);
     return cudaGetLastError();
 }
 

@@ -58,3 +58,27 @@ def rope_table(max_position: int = wl.MAX_POSITION, base: float = wl.ROPE_BASE) 
     t = torch.empty(max_position, 128, dtype=torch.float32, device="cuda")
     nv.nv_rope_cos_sin_cache(t, base)
     return t
+
+
+# K rows reach the cache after the GPU rounds its fp32 rotation to bf16 and
+# the oracle rounds its fp64 one.  Away from zero the two differ by at most
+# one bf16 ulp (2^-7 |r| bounds it).  Near zero the rotation x*cos - y*sin
+# cancels: its fp32 error scales with the terms (|x|, |y| ~ 1 after the
+# norm; norm, table and products cost a few 2^-24 each, 1e-6 at worst), not
+# with the small result, so an absolute 2^-16 is allowed on top.  A wrong
+# sign, index or weight moves values by O(1) and still fails.
+CACHE_ABS_TOL = 2.0 ** -16
+
+
+def check_cache_rows(gpu_bits: np.ndarray, ref_bits: np.ndarray, what: str,
+                     max_mismatch_frac: float = 0.01) -> None:
+    g = wl.bf16_bits_to_f32(gpu_bits).astype(np.float64)
+    r = wl.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    diff = np.abs(g - r)
+    bad = diff > 2.0 ** -7 * np.abs(r) + CACHE_ABS_TOL
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        worst = [(tuple(int(v) for v in i), float(g[tuple(i)]), float(r[tuple(i)])) for i in idx]
+        raise AssertionError(f"{what}: {int(bad.sum())} elements beyond one ulp; first {worst}")
+    frac = float(np.mean(gpu_bits != ref_bits))
+    assert frac < max_mismatch_frac, f"{what}: {frac:.4%} of elements differ by one ulp"

@@ -159,3 +159,25 @@ def test_paged_prefill_rejects_bad_arguments(lib):
     assert call(Hq=12) == NV_EINVAL
     assert call(q=MIS) == NV_EALIGN
     assert call(B=0) == NV_OK
+
+
+def test_qknorm_rope_store_rejects_bad_arguments(lib):
+    f = lib.nv_qknorm_rope_store
+    ok = dict(q=FAKE, qs=6144, k=FAKE, ks=6144, v=FAKE, vs=6144, sm=FAKE, kc=FAKE, vc=FAKE,
+              ns=1 << 20, T=4, Hq=32, Hkv=8, d=128, wk=0)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q"], a["qs"], a["k"], a["ks"], a["v"], a["vs"], FAKE, FAKE, FAKE, 40960, FAKE,
+                 a["sm"], a["kc"], a["vc"], a["ns"], a["T"], a["Hq"], a["Hkv"], a["d"], 1e-6,
+                 a["wk"], None, None)
+
+    assert call(d=64) == NV_EUNSUPPORTED
+    assert call(sm=None) == NV_EINVAL
+    assert call(vc=None) == NV_EINVAL
+    assert call(vs=512) == NV_EINVAL                 # stride shorter than Hkv * d
+    assert call(wk=2) == NV_EINVAL
+    assert call(ns=-1) == NV_EINVAL
+    assert call(kc=MIS) == NV_EALIGN
+    assert call(vs=6148) == NV_EALIGN
+    assert call(T=0) == NV_OK
