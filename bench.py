@@ -338,8 +338,39 @@ def run_ours(args, rank, world, local_rank):
 
     graph_info = graph_decode_overhead(dev_t)
 
+    # ---- QK-Norm + RoPE + store on the prefill batch: two kernels vs one pass
+    def time_us(fn, reps=20):
+        for _ in range(3):
+            fn()
+        e0, e1 = ev(), ev()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def pair():
+        nv.nv_qknorm_rope(pq, pk, p_qn, p_kn, table, p_pos, eps=wl.RMS_EPS, err_count=err)
+        nv.nv_store_kvcache(pk, pv, pkc, pvc, p_slots, err)
+
+    def fused():
+        nv.nv_qknorm_rope_store(pq, pk, pv, p_qn, p_kn, table, p_pos, pkc, pvc, p_slots,
+                                eps=wl.RMS_EPS, write_k=True, err_count=err)
+
+    pair_us, fused_us = time_us(pair), time_us(fused)
+    # q and k read and written by the rotation, k and v read and written by the store;
+    # the fused pass reads q, k, v once and writes q, k and both cache rows.
+    pair_bytes = T * (2 * (Q + D) + 4 * D) * 2
+    fused_bytes = T * ((Q + 2 * D) + (Q + D) + 2 * D) * 2
+    rope_store = {"tokens": T, "write_k": True, "pair_us": pair_us, "fused_us": fused_us,
+                  "pair_bytes": pair_bytes, "fused_bytes": fused_bytes,
+                  "fused_gbs": fused_bytes / (fused_us * 1e-6) / 1e9,
+                  "pair_gbs": pair_bytes / (pair_us * 1e-6) / 1e9}
+    assert int(err.item()) == 0, f"device error count {int(err.item())}"
+
     return dict(
-        graph=graph_info,
+        graph=graph_info, rope_store=rope_store,
         value=value, ms_per_step=tot_ms / args.steps, dec_ms=statistics.mean(dec_ms),
         pre_ms=statistics.mean(pre_ms), attn_ms=statistics.mean(attn_ms),
         attn_gbs=attn_gbs, ptflops=ptflops, pattn_ms=pattn_sum / args.steps, clocks=clk,
@@ -349,19 +380,17 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------ launch overhead: CUDA graph
-def graph_decode_overhead(dev_t, reps: int = 200):
-    """A small decode layer step (Qwen3-8B heads, bucket of 8 rows, 6 real
-    sequences of ~2k keys, 2 padded rows with slot -1 and ctx 0): the four
-    ABI calls timed eagerly and as one captured CUDA graph replay."""
+def graph_decode_overhead(dev_t, buckets=(1, 8, 64, 512), ctx_len: int = 1024, reps: int = 100):
+    """The decode layer's four ABI calls (Qwen3-8B heads) timed eagerly and as
+    one captured CUDA graph per batch bucket.  Every sequence has ctx_len keys;
+    buckets above 2 end with two padded rows (slot -1, context length 0)."""
     import torch
     import paged_kv_attention_kvcache_gb300 as nv
     s = wl.QWEN3_8B
-    bucket, n_real = 8, 6
-    ctx = np.zeros(bucket, np.int32)
-    ctx[:n_real] = 2048
-    step = wl.make_decode(77, s, np.maximum(ctx, 1), 8 * 8 + 2, with_norms=True, name="graph")
-    step.context_lens[:] = ctx
-    step.slot_mapping[n_real:] = -1
+    nmax = max(buckets)
+    blocks = -(-ctx_len // wl.BLOCK_SIZE)
+    step = wl.make_decode(77, s, np.full(nmax, ctx_len, np.int32), nmax * blocks + 2,
+                          with_norms=True, name="graph")
     Q, D = s.q_size, s.kv_size
 
     def dev(bits):
@@ -371,55 +400,65 @@ def graph_decode_overhead(dev_t, reps: int = 200):
     table = torch.empty(wl.MAX_POSITION, 128, dtype=torch.float32, device=dev_t)
     nv.nv_rope_cos_sin_cache(table, wl.ROPE_BASE)
     kc, vc = dev(step.pool.k), dev(step.pool.v)
-    x, r, g = dev(step.x), dev(step.residual), dev(step.gamma)
-    y = torch.empty_like(x)
-    qkv = dev(step.qkv)
-    qn, kn = dev(step.q_norm_w), dev(step.k_norm_w)
-    pos = torch.from_numpy(step.positions).to(dev_t)
-    slots = torch.from_numpy(step.slot_mapping).to(dev_t)
-    bt = torch.from_numpy(step.block_tables).to(dev_t)
-    cl = torch.from_numpy(step.context_lens).to(dev_t)
-    o = torch.empty(bucket, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
-    wsb = nv.nv_decode_attn_workspace_size(bucket, s.hq, s.hkv, 128, bt.shape[1], 256, 0)
-    ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
-    q = qkv[:, :Q].view(bucket, s.hq, 128)
-    k = qkv[:, Q:Q + D].view(bucket, s.hkv, 128)
-    v = qkv[:, Q + D:].view(bucket, s.hkv, 128)
+    g, qn, kn = dev(step.gamma), dev(step.q_norm_w), dev(step.k_norm_w)
+    out = []
+    for b in buckets:
+        n_real = b - 2 if b > 2 else b
+        ctx = step.context_lens[:b].copy()
+        slots = step.slot_mapping[:b].copy()
+        ctx[n_real:] = 0
+        slots[n_real:] = -1
+        x, r = dev(step.x[:b]), dev(step.residual[:b])
+        y = torch.empty_like(x)
+        qkv = dev(step.qkv[:b])
+        d_pos = torch.from_numpy(step.positions[:b].copy()).to(dev_t)
+        d_slots = torch.from_numpy(slots).to(dev_t)
+        d_bt = torch.from_numpy(step.block_tables[:b].copy()).to(dev_t)
+        d_ctx = torch.from_numpy(ctx).to(dev_t)
+        o = torch.empty(b, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
+        wsb = nv.nv_decode_attn_workspace_size(b, s.hq, s.hkv, 128, d_bt.shape[1],
+                                               wl.BLOCK_SIZE, 0)
+        ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
+        q = qkv[:, :Q].view(b, s.hq, 128)
+        k = qkv[:, Q:Q + D].view(b, s.hkv, 128)
+        v = qkv[:, Q + D:].view(b, s.hkv, 128)
 
-    def layer():
-        nv.nv_add_rmsnorm(x, r, g, y, r, eps=wl.RMS_EPS)
-        nv.nv_qknorm_rope(q, k, qn, kn, table, pos, eps=wl.RMS_EPS)
-        nv.nv_store_kvcache(k, v, kc, vc, slots)
-        nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws)
+        def layer():
+            nv.nv_add_rmsnorm(x, r, g, y, r, eps=wl.RMS_EPS)
+            nv.nv_qknorm_rope(q, k, qn, kn, table, d_pos, eps=wl.RMS_EPS)
+            nv.nv_store_kvcache(k, v, kc, vc, d_slots)
+            nv.nv_decode_attn_paged(q, kc, vc, d_bt, d_ctx, o, SCALE, workspace=ws)
 
-    side = torch.cuda.Stream(device=dev_t)
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        for _ in range(3):
+        side = torch.cuda.Stream(device=dev_t)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                layer()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
             layer()
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        layer()
 
-    def timed(fn):
-        for _ in range(10):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / reps
+        def timed(fn):
+            for _ in range(10):
+                fn()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / reps
 
-    eager_us = timed(layer)
-    graph_us = timed(graph.replay)
-    return {"batch_bucket": bucket, "real_sequences": n_real, "ctx": 2048,
-            "eager_us_per_step": eager_us, "graph_us_per_step": graph_us,
-            "kernels_per_step": 4 + (1 if wsb else 0)}
+        eager_us = timed(layer)
+        graph_us = timed(graph.replay)
+        out.append({"bucket": b, "real": n_real, "eager_us": round(eager_us, 2),
+                    "graph_us": round(graph_us, 2), "kernels": 4 + (1 if wsb else 0)})
+        del graph
+    return {"ctx": ctx_len, "heads": "32/8", "per_bucket": out}
 
 
 # ------------------------------------------------------------ oracle side
@@ -600,6 +639,7 @@ def main():
             "e2e": {"value": r["e2e"], "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]},
             "decode_graph": r["graph"],
+            "rope_store_prefill": r["rope_store"],
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
