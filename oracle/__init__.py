@@ -64,6 +64,8 @@ def _load():
             lib.orc_qknorm_rope.restype = _I32
             lib.orc_store_kvcache.argtypes = [_P, _I64, _P, _I64, _P, _P, _P, _I64, _I64, _I64]
             lib.orc_store_kvcache.restype = _I64
+            lib.orc_silu_and_mul.argtypes = [_P, _I64, _I64, _I64, _P]
+            lib.orc_silu_and_mul.restype = _I32
             lib.orc_attention_varlen.argtypes = [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I32,
                                                  _I32, _I32, _I32, _F64, _I32, _P, _I64, _P]
             lib.orc_attention_varlen.restype = _I32
@@ -171,6 +173,23 @@ def store_kvcache(key, value, k_cache, v_cache, slot_mapping) -> int:
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int32)
     return int(_load().orc_store_kvcache(_ptr(key), D, _ptr(value), D, _ptr(k_cache),
                                          _ptr(v_cache), _ptr(slots), N, D, num_slots))
+
+
+def silu_and_mul(x):
+    """SwiGLU activation ("3.3 Model skeleton and core operators", sec. 4).
+
+    x: [T, 2I] bf16 bits, gate in the first half, up in the second.  Returns
+    silu(gate) * up as [T, I] fp64 (unrounded).
+    """
+    x = _u16(x)
+    if x.ndim != 2 or x.shape[1] % 2:
+        raise ValueError("x must be [T, 2I]")
+    T, two_i = x.shape
+    out = np.empty((T, two_i // 2), dtype=np.float64)
+    rc = _load().orc_silu_and_mul(_ptr(x), two_i, T, two_i // 2, _ptr(out))
+    if rc:
+        raise ValueError("orc_silu_and_mul: bad arguments")
+    return out
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = True,

@@ -29,6 +29,8 @@
  *           softmax(QK^T * scale) V); "同一个 Qwen3，两种写法", sec. 3.2
  *           (packed varlen layout, block-diagonal causal mask) and sec. 3.4
  *           (GQA handled inside the kernel, no repeat_kv).
+ *   [SWIGLU] "3.3 Model skeleton and core operators", sec. 4 SwiGLU:
+ *           SiluAndMul (gate first, up second) and sec. 5 (Qwen3MLP).
  *   [PAGED] "nano-vllm code walkthrough", Prefill stage case 2 and Decode
  *           Stage (block_table "stitches" physical blocks into the logical
  *           K/V sequence; cache_seqlens = current length of each sequence).
@@ -218,6 +220,27 @@ int64_t orc_store_kvcache(const uint16_t *key, int64_t key_stride,
         memcpy(v_cache + slot * D, value + n * value_stride, (size_t)D * sizeof(uint16_t));
     }
     return bad;
+}
+
+/*
+ * [SWIGLU] SiluAndMul: row t of x holds 2*I values, the first I the gate g
+ * and the last I the up projection u (the merged gate_up output, split in
+ * half along the last dim, gate first).  out[t][i] = silu(g_i) * u_i with
+ * silu(g) = g / (1 + exp(-g)).  The pages run it under torch.compile, which
+ * fuses the two ops; the plain reading is one value per element, rounded
+ * once at the end, so it is returned unrounded here.
+ */
+int orc_silu_and_mul(const uint16_t *x, int64_t x_stride, int64_t T, int64_t I, double *out) {
+    if (T < 0 || I < 0 || x_stride < 2 * I) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < I; ++i) {
+            double g = bf16_bits_to_double(x[t * x_stride + i]);
+            double u = bf16_bits_to_double(x[t * x_stride + I + i]);
+            out[t * I + i] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+    return 0;
 }
 
 /*

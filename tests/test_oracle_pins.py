@@ -472,3 +472,48 @@ def test_paged_prefill_single_query_is_paged_decode_and_prefix_mean():
         mean = F32(np.stack(rows)).astype(np.float64).mean(0)
         for h in range(hq):
             np.testing.assert_allclose(out[i, h], mean[h // (hq // hkv)], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- SiluAndMul
+def _bits(values):
+    return wl.f32_to_bf16_bits(np.asarray(values, dtype=np.float32))
+
+
+def test_silu_and_mul_gate_first_and_limits():
+    # "3.3 Model skeleton and core operators", sec. 4: the first half of the
+    # merged projection is the gate, the second the up projection.  A large
+    # positive gate passes up through (silu(g) -> g), a large negative one
+    # closes it (silu(g) -> 0); swapping the halves changes both results.
+    x = _bits([[30.0, 1.0], [-30.0, 5.0], [0.0, 7.0], [1.0, 0.0]])
+    out = oracle.silu_and_mul(x)
+    assert out.shape == (4, 1)
+    assert 0 < 30.0 - out[0, 0] < 30 * math.exp(-30)      # 30 * sigmoid(30) * 1
+    assert 0 < -out[1, 0] < 5 * 30 * math.exp(-30)        # gate closed
+    assert out[2, 0] == 0.0 and out[3, 0] == 0.0  # silu(0) = 0; up = 0
+
+
+def test_silu_and_mul_odd_even_identities():
+    # silu(g) - silu(-g) = g   and   silu(g) + silu(-g) = g * tanh(g / 2),
+    # the second against numpy's tanh: a sign slip in the exponent flips it.
+    g = wl.bf16_bits_to_f32(_bits(np.linspace(-9.0, 9.0, 37))).astype(np.float64)
+    up = np.ones_like(g)
+    pos = oracle.silu_and_mul(_bits(np.stack([g, up], 1)))[:, 0]
+    neg = oracle.silu_and_mul(_bits(np.stack([-g, up], 1)))[:, 0]
+    assert np.allclose(pos - neg, g, rtol=0, atol=1e-14)
+    assert np.allclose(pos + neg, g * np.tanh(g / 2), rtol=0, atol=1e-14)
+
+
+def test_silu_and_mul_matches_torch_fp64_and_page_toy_shape():
+    # The toy MLP of the page: [5, 2I/TP] = [5, 16] in, [5, 8] out.  Values
+    # against torch's own silu in fp64 on the CPU (an independent routine).
+    torch = pytest.importorskip("torch")
+    x = wl.normal_bf16(41, "pin.swiglu", (5, 16), 0.0, 2.0)
+    out = oracle.silu_and_mul(x)
+    assert out.shape == (5, 8)
+    xf = torch.from_numpy(wl.bf16_bits_to_f32(x).astype(np.float64))
+    ref = torch.nn.functional.silu(xf[:, :8]) * xf[:, 8:]
+    assert np.allclose(out, ref.numpy(), rtol=1e-14, atol=1e-15)
+    # up is a plain multiplier
+    x2 = x.copy()
+    x2[:, 8:] = _bits(2.0 * wl.bf16_bits_to_f32(x[:, 8:]))
+    assert np.allclose(oracle.silu_and_mul(x2), 2.0 * out, rtol=1e-15, atol=0)
