@@ -369,8 +369,18 @@ def run_ours(args, rank, world, local_rank):
                   "pair_gbs": pair_bytes / (pair_us * 1e-6) / 1e9}
     assert int(err.item()) == 0, f"device error count {int(err.item())}"
 
+    # ---- the MLP's SiluAndMul on the prefill batch (Qwen3-8B intermediate 12288)
+    inter = 12288
+    gate_up = torch.empty(T, 2 * inter, dtype=torch.bfloat16, device=dev_t).normal_()
+    act = torch.empty(T, inter, dtype=torch.bfloat16, device=dev_t)
+    swiglu_us = time_us(lambda: nv.nv_silu_and_mul(gate_up, act))
+    swiglu_bytes = T * 3 * inter * 2
+    swiglu = {"tokens": T, "intermediate": inter, "us": swiglu_us, "bytes": swiglu_bytes,
+              "gbs": swiglu_bytes / (swiglu_us * 1e-6) / 1e9}
+    del gate_up, act
+
     return dict(
-        graph=graph_info, rope_store=rope_store,
+        graph=graph_info, rope_store=rope_store, swiglu=swiglu,
         value=value, ms_per_step=tot_ms / args.steps, dec_ms=statistics.mean(dec_ms),
         pre_ms=statistics.mean(pre_ms), attn_ms=statistics.mean(attn_ms),
         attn_gbs=attn_gbs, ptflops=ptflops, pattn_ms=pattn_sum / args.steps, clocks=clk,
@@ -640,6 +650,7 @@ def main():
                     "d2h_bytes_per_step": r["d2h"]},
             "decode_graph": r["graph"],
             "rope_store_prefill": r["rope_store"],
+            "silu_and_mul_prefill": r["swiglu"],
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }

@@ -10,6 +10,7 @@
  *   nv_prefill_attn_varlen  causal GQA attention over packed sequences
  *   nv_prefill_attn_paged   the same with K/V read through the block table
  *   nv_decode_attn_paged    single-query GQA attention over the paged cache
+ *   nv_silu_and_mul         the MLP's SwiGLU activation that follows the sublayer
  * plus nv_rope_cos_sin_cache (builds the RoPE table once) and the decode
  * workspace query.
  *
@@ -191,6 +192,26 @@ NV_API int nv_qknorm_rope_store(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k
                                 nv_bf16_t *v_cache, int64_t num_slots, int64_t T, int Hq,
                                 int Hkv, int head_dim, float eps, int write_k,
                                 int *err_count, void *stream);
+
+/*
+ * SiluAndMul, the SwiGLU activation of the MLP that follows the attention
+ * sublayer.  "3.3 Model skeleton and core operators", sec. 4 (SwiGLU:
+ * SiluAndMul splits the merged gate_up output in half along the last dim,
+ * gate first) and sec. 5 (Qwen3MLP: gate_up_proj -> act_fn -> down_proj).
+ * With I = intermediate:
+ *   out[t][i] = bf16( silu(x[t][i]) * x[t][I + i] ),  silu(g) = g / (1 + e^-g)
+ * in fp32 with one rounding at the end (the pages run it under
+ * torch.compile, which fuses the two ops).
+ *   x    [T, 2I] bf16, token stride x_tok_stride (>= 2I).
+ *   out  [T, I] bf16, token stride out_tok_stride (>= I), written.
+ * out may equal x when the two strides are equal (the result then fills the
+ * gate half); any other overlap is rejected with NV_EINVAL.  Requires
+ * I % 8 == 0, strides multiples of 8, 16-byte aligned pointers.  T == 0 or
+ * I == 0 is a no-op.
+ */
+NV_API int nv_silu_and_mul(const nv_bf16_t *x, int64_t x_tok_stride, nv_bf16_t *out,
+                           int64_t out_tok_stride, int64_t T, int intermediate,
+                           void *stream);
 
 /*
  * Varlen causal prefill attention.  "3.3 Model skeleton and core

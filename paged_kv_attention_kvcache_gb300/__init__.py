@@ -27,13 +27,14 @@ __all__ = [
     "NvAttnError", "library", "library_path", "nv_version",
     "nv_rope_cos_sin_cache", "nv_add_rmsnorm", "nv_qknorm_rope", "nv_store_kvcache",
     "nv_qknorm_rope_store", "nv_prefill_attn_varlen", "nv_prefill_attn_paged", "nv_decode_attn_workspace_size",
-    "nv_decode_attn_paged", "ABI_FUNCTIONS",
+    "nv_decode_attn_paged", "nv_silu_and_mul", "ABI_FUNCTIONS",
 ]
 
 ABI_FUNCTIONS = (
     "nv_status_string", "nv_version", "nv_rope_cos_sin_cache", "nv_add_rmsnorm",
     "nv_qknorm_rope", "nv_store_kvcache", "nv_qknorm_rope_store", "nv_prefill_attn_varlen",
-    "nv_prefill_attn_paged", "nv_decode_attn_workspace_size", "nv_decode_attn_paged", "nv_decode_attn_paged_noalloc",
+    "nv_prefill_attn_paged", "nv_decode_attn_workspace_size", "nv_decode_attn_paged",
+    "nv_decode_attn_paged_noalloc", "nv_silu_and_mul",
 )
 
 _P, _I64, _I32, _F32, _F64, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -52,6 +53,7 @@ _SIGNATURES = {
                                 _I32, _I32, _I32, _I32, _F32, _I32, _P, _P], _I32),
     "nv_prefill_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _I64, _I32, _I32, _I32,
                                _I32, _I32, _I64, _F32, _I32, _P, _P], _I32),
+    "nv_silu_and_mul": ([_P, _I64, _P, _I64, _I64, _I32, _P], _I32),
     "nv_decode_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "nv_decode_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32,
                               _I64, _F32, _I32, _P, _SZ, _P, _P], _I32),
@@ -236,3 +238,15 @@ def nv_decode_attn_paged(q, k_cache, v_cache, block_tables, context_lens, o,
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), _ptr(o), B, Hq, Hkv, d, bs, nb, float(softmax_scale),
         int(kv_split_tokens), _ptr(workspace), ws_bytes, _ptr(err_count), _stream(stream)))
+
+
+def nv_silu_and_mul(x, out, stream=None) -> None:
+    """out [T, I] = silu(x[:, :I]) * x[:, I:] for x [T, 2I] (row-strided views
+    allowed; out may be x[:, :I] itself)."""
+    if x.dim() != 2 or out.dim() != 2 or x.stride(1) != 1 or out.stride(1) != 1:
+        raise ValueError("silu_and_mul takes [T, 2I] and [T, I] row-major views")
+    T, two_i = x.shape
+    if two_i % 2 or tuple(out.shape) != (T, two_i // 2):
+        raise ValueError("out must be [T, I] for x [T, 2I]")
+    _check("nv_silu_and_mul", library().nv_silu_and_mul(
+        _ptr(x), x.stride(0), _ptr(out), out.stride(0), T, two_i // 2, _stream(stream)))

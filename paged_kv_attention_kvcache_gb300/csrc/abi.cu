@@ -185,6 +185,26 @@ int nv_qknorm_rope_store(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
         write_k, err_count, as_stream(stream)));
 }
 
+int nv_silu_and_mul(const nv_bf16_t *x, int64_t x_tok_stride, nv_bf16_t *out,
+                    int64_t out_tok_stride, int64_t T, int intermediate, void *stream) {
+    if (T < 0 || intermediate < 0) return NV_EINVAL;
+    if (intermediate % 8) return NV_EUNSUPPORTED;
+    if (T == 0 || intermediate == 0) return NV_OK;
+    if (!x || !out) return NV_EINVAL;
+    if (x_tok_stride < 2 * (int64_t)intermediate || out_tok_stride < intermediate)
+        return NV_EINVAL;
+    if (x_tok_stride % 8 || out_tok_stride % 8 || !aligned16(x) || !aligned16(out))
+        return NV_EALIGN;
+    // The only overlap allowed is out == x with the same token stride.
+    const uintptr_t x0 = (uintptr_t)x, o0 = (uintptr_t)out;
+    const uintptr_t x1 = x0 + (uintptr_t)(((T - 1) * x_tok_stride + 2 * (int64_t)intermediate) * 2);
+    const uintptr_t o1 = o0 + (uintptr_t)(((T - 1) * out_tok_stride + intermediate) * 2);
+    const bool overlap = x0 < o1 && o0 < x1;
+    if (overlap && !(o0 == x0 && out_tok_stride == x_tok_stride)) return NV_EINVAL;
+    return launch_status(launch_silu_and_mul(x, x_tok_stride, out, out_tok_stride, T,
+                                             intermediate, as_stream(stream)));
+}
+
 int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf16_t *k,
                            int64_t k_tok_stride, const nv_bf16_t *v, int64_t v_tok_stride,
                            nv_bf16_t *o, const int32_t *cu_seqlens_q,

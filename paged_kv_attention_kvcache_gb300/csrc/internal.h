@@ -32,6 +32,9 @@ cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
                                      int64_t T, int Hq, int Hkv, float eps, int write_k,
                                      int *err_count, cudaStream_t s);
 
+cudaError_t launch_silu_and_mul(const uint16_t *x, int64_t x_stride, uint16_t *out,
+                                int64_t out_stride, int64_t T, int I, cudaStream_t s);
+
 cudaError_t launch_store_kvcache(const uint16_t *key, int64_t key_stride, const uint16_t *value,
                                  int64_t value_stride, uint16_t *k_cache, uint16_t *v_cache,
                                  const int32_t *slot_mapping, int64_t N, int D,

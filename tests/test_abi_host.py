@@ -41,8 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
     for name in names:
         assert hasattr(lib, name), name
-    assert set(names) <= set(nv.ABI_FUNCTIONS) | set(names)
-    assert set(nv.ABI_FUNCTIONS) <= set(names)
+    assert set(names) == set(nv.ABI_FUNCTIONS)
 
 
 def test_status_strings_and_version(lib):
@@ -181,3 +180,18 @@ def test_qknorm_rope_store_rejects_bad_arguments(lib):
     assert call(kc=MIS) == NV_EALIGN
     assert call(vs=6148) == NV_EALIGN
     assert call(T=0) == NV_OK
+
+
+def test_silu_and_mul_rejects_bad_arguments(lib):
+    f = lib.nv_silu_and_mul
+    X, O = 0x100000, 0x900000                         # far apart: no overlap
+    assert f(X, 24576, O, 12288, 4, 12280 + 4, None) == NV_EUNSUPPORTED   # I % 8
+    assert f(None, 24576, O, 12288, 4, 12288, None) == NV_EINVAL
+    assert f(X, 24570, O, 12288, 4, 12288, None) == NV_EINVAL            # stride < 2I
+    assert f(X, 24576, O, 12280, 4, 12288, None) == NV_EINVAL            # out stride < I
+    assert f(X + 2, 24576, O, 12288, 4, 12288, None) == NV_EALIGN
+    assert f(X, 24584 + 4, O, 12288, 4, 12288, None) == NV_EALIGN
+    assert f(X, 24576, X + 2 * 12288 * 2, 12288, 4, 12288, None) == NV_EINVAL  # overlap
+    assert f(X, 24576, X, 12288, 4, 12288, None) == NV_EINVAL      # same base, other stride
+    assert f(X, 24576, O, 12288, 0, 12288, None) == NV_OK
+    assert f(X, 24576, O, 12288, -1, 12288, None) == NV_EINVAL
