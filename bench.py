@@ -231,6 +231,7 @@ def run_ours(args, rank, world, local_rank):
     pq, pk, pv = (p_qkv[:, :Q].view(T, s.hq, 128), p_qkv[:, Q:Q + D].view(T, s.hkv, 128),
                   p_qkv[:, Q + D:].view(T, s.hkv, 128))
     max_len = int(pre.lengths.max())
+    p_sched = torch.zeros(1, dtype=torch.int32, device=dev_t)   # dynamic work counter
 
     def prefill_layer(ev=None):
         nv.nv_add_rmsnorm(p_x, p_r, p_g, p_y, p_r, eps=wl.RMS_EPS)
@@ -239,7 +240,7 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[0].record()
         nv.nv_prefill_attn_varlen(pq, pk, pv, p_o, p_cu, p_cu, max_len, max_len, SCALE,
-                                  err_count=err)
+                                  err_count=err, sched_counter=p_sched)
         if ev:
             ev[1].record()
 
@@ -571,8 +572,9 @@ def run_ncu_case(which: str, launches: int = 3):
                    qkv[:, Q + D:].view(T, s.hkv, 128))
         cu = torch.from_numpy(pre.cu_seqlens).cuda()
         o = torch.empty(T, s.hq, 128, dtype=torch.bfloat16, device="cuda")
+        sched = torch.zeros(1, dtype=torch.int32, device="cuda")
         for _ in range(launches):
-            nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, 2048, 2048, SCALE)
+            nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, 2048, 2048, SCALE, sched_counter=sched)
     torch.cuda.synchronize()
     print(f"ncu case {which}: {launches} launches done")
 

@@ -240,6 +240,12 @@ NV_API int nv_silu_and_mul(const nv_bf16_t *x, int64_t x_tok_stride, nv_bf16_t *
  * Requires head_dim == 128, token strides multiples of 8, 16-byte aligned
  * pointers, total_q, total_k < 2^31.  err_count (optional) counts skipped
  * sequences and records NV_ERR_PIPELINE_FAILURE.
+ * sched_counter (optional, recommended): one int of device memory, 4-byte
+ * aligned, through which the persistent CTAs draw work items heaviest first
+ * (an atomic counter), which balances ragged batches.  The call clears it
+ * with an enqueued memset before its kernel, so its contents on entry do
+ * not matter, but calls that may run concurrently need distinct counters.
+ * NULL gives a fixed round-robin assignment of items to CTAs.
  */
 NV_API int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
                            const nv_bf16_t *k, int64_t k_tok_stride,
@@ -248,7 +254,8 @@ NV_API int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
                            const int32_t *cu_seqlens_k, int B, int64_t total_q,
                            int64_t total_k, int max_seqlen_q, int max_seqlen_k,
                            int Hq, int Hkv, int head_dim, float softmax_scale,
-                           int causal, int *err_count, void *stream);
+                           int causal, int *sched_counter, int *err_count,
+                           void *stream);
 
 /*
  * Prefill over the paged cache: a prefix-cache hit, or a later chunk of a
@@ -270,7 +277,8 @@ NV_API int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride,
  * zeros; a sequence with Lk < Lq or Lk > max_blocks_per_seq * block_size is
  * skipped and counted.  Cache rows past Lk may hold any bits.  Requires
  * head_dim == 128, block_size % 128 == 0, causal == 1, 16-byte aligned
- * pointers, q_tok_stride a multiple of 8.
+ * pointers, q_tok_stride a multiple of 8.  sched_counter as for
+ * nv_prefill_attn_varlen.
  */
 NV_API int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
                                  const nv_bf16_t *k_cache, const nv_bf16_t *v_cache,
@@ -279,7 +287,8 @@ NV_API int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
                                  const int32_t *cu_seqlens_k, int B, int64_t total_q,
                                  int max_seqlen_q, int Hq, int Hkv, int head_dim,
                                  int block_size, int64_t num_blocks, float softmax_scale,
-                                 int causal, int *err_count, void *stream);
+                                 int causal, int *sched_counter, int *err_count,
+                                 void *stream);
 
 /*
  * Bytes of fp32 workspace nv_decode_attn_paged needs for these sizes and

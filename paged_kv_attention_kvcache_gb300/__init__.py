@@ -50,9 +50,9 @@ _SIGNATURES = {
     "nv_qknorm_rope_store": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _P, _P, _P, _I64,
                               _I64, _I32, _I32, _I32, _F32, _I32, _P, _P], _I32),
     "nv_prefill_attn_varlen": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I32, _I64, _I64, _I32,
-                                _I32, _I32, _I32, _I32, _F32, _I32, _P, _P], _I32),
+                                _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P], _I32),
     "nv_prefill_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _I64, _I32, _I32, _I32,
-                               _I32, _I32, _I64, _F32, _I32, _P, _P], _I32),
+                               _I32, _I32, _I64, _F32, _I32, _P, _P, _P], _I32),
     "nv_silu_and_mul": ([_P, _I64, _P, _I64, _I64, _I32, _P], _I32),
     "nv_decode_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "nv_decode_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32,
@@ -186,8 +186,10 @@ def nv_qknorm_rope_store(q, k, v, q_norm_weight, k_norm_weight, cos_sin, positio
 
 def nv_prefill_attn_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                            max_seqlen_k: int, softmax_scale: float, causal: bool = True,
-                           err_count=None, stream=None) -> None:
-    """Varlen causal attention; o [Tq, Hq, 128] contiguous is written."""
+                           err_count=None, stream=None, sched_counter=None) -> None:
+    """Varlen causal attention; o [Tq, Hq, 128] contiguous is written.
+    sched_counter: optional int32 device tensor (one element) that lets the
+    CTAs draw work heaviest first; None gives the round-robin assignment."""
     qs = _heads_view(q, "q")
     ks = _heads_view(k, "k")
     vs = _heads_view(v, "v")
@@ -198,12 +200,13 @@ def nv_prefill_attn_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q:
     _check("nv_prefill_attn_varlen", library().nv_prefill_attn_varlen(
         _ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(o), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
         B, Tq, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), Hq, k.shape[1], d,
-        float(softmax_scale), 1 if causal else 0, _ptr(err_count), _stream(stream)))
+        float(softmax_scale), 1 if causal else 0, _ptr(sched_counter), _ptr(err_count),
+        _stream(stream)))
 
 
 def nv_prefill_attn_paged(q, k_cache, v_cache, block_tables, o, cu_seqlens_q, cu_seqlens_k,
                           max_seqlen_q: int, softmax_scale: float, causal: bool = True,
-                          err_count=None, stream=None) -> None:
+                          err_count=None, stream=None, sched_counter=None) -> None:
     """Prefill whose keys (cached prefix + new tokens) are read from the paged
     cache through block_tables; o [Tq, Hq, 128] contiguous is written."""
     qs = _heads_view(q, "q")
@@ -215,7 +218,8 @@ def nv_prefill_attn_paged(q, k_cache, v_cache, block_tables, o, cu_seqlens_q, cu
     _check("nv_prefill_attn_paged", library().nv_prefill_attn_paged(
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(o), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Tq, int(max_seqlen_q), Hq, Hkv, d,
-        bs, nb, float(softmax_scale), 1 if causal else 0, _ptr(err_count), _stream(stream)))
+        bs, nb, float(softmax_scale), 1 if causal else 0, _ptr(sched_counter), _ptr(err_count),
+        _stream(stream)))
 
 
 def nv_decode_attn_workspace_size(B, Hq, Hkv, head_dim, max_blocks_per_seq, block_size,

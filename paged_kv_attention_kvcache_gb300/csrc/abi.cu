@@ -210,7 +210,8 @@ int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf
                            nv_bf16_t *o, const int32_t *cu_seqlens_q,
                            const int32_t *cu_seqlens_k, int B, int64_t total_q, int64_t total_k,
                            int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int head_dim,
-                           float softmax_scale, int causal, int *err_count, void *stream) {
+                           float softmax_scale, int causal, int *sched_counter, int *err_count,
+                           void *stream) {
     if (B < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
         Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !(softmax_scale > 0.f) || !isfinite(softmax_scale))
         return NV_EINVAL;
@@ -223,7 +224,7 @@ int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf
         v_tok_stride < (int64_t)Hkv * 128)
         return NV_EINVAL;
     if (q_tok_stride % 8 || k_tok_stride % 8 || v_tok_stride % 8 || !aligned16(q) ||
-        !aligned16(k) || !aligned16(v) || !aligned16(o))
+        !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)sched_counter & 3))
         return NV_EALIGN;
     if ((int64_t)(max_seqlen_q + 127) / 128 > 65535) return NV_EUNSUPPORTED;
 
@@ -251,6 +252,7 @@ int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf
     p.max_seqlen_q = max_seqlen_q;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.err_count = err_count;
+    p.work_counter = sched_counter;
     p.block_tables = nullptr;
     p.max_blocks = 0;
     p.block_size = 0;
@@ -263,7 +265,8 @@ int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf1
                           int max_blocks_per_seq, nv_bf16_t *o, const int32_t *cu_seqlens_q,
                           const int32_t *cu_seqlens_k, int B, int64_t total_q, int max_seqlen_q,
                           int Hq, int Hkv, int head_dim, int block_size, int64_t num_blocks,
-                          float softmax_scale, int causal, int *err_count, void *stream) {
+                          float softmax_scale, int causal, int *sched_counter, int *err_count,
+                          void *stream) {
     if (B < 0 || total_q < 0 || max_seqlen_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
         max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0 ||
         !(softmax_scale > 0.f) || !isfinite(softmax_scale))
@@ -277,7 +280,7 @@ int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf1
         return NV_EINVAL;
     if (q_tok_stride < (int64_t)Hq * 128) return NV_EINVAL;
     if (q_tok_stride % 8 || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-        !aligned16(o))
+        !aligned16(o) || ((uintptr_t)sched_counter & 3))
         return NV_EALIGN;
     if ((int64_t)(max_seqlen_q + 127) / 128 > 65535) return NV_EUNSUPPORTED;
 
@@ -307,6 +310,7 @@ int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf1
     p.max_seqlen_q = max_seqlen_q;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.err_count = err_count;
+    p.work_counter = sched_counter;
     p.block_tables = block_tables;
     p.max_blocks = max_blocks_per_seq;
     p.block_size = block_size;

@@ -75,6 +75,7 @@ struct PrefillParams {
     int max_seqlen_q;
     float scale_log2;
     int *err_count;
+    int *work_counter;         // optional: items handed out by atomicAdd (cleared per launch)
     // Paged K/V only: keys come from the cache through the block table.
     const int32_t *block_tables;
     int max_blocks;

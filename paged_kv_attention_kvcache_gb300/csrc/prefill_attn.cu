@@ -8,10 +8,14 @@
 // inside each; keys of other sequences are never admitted.
 //
 // How (GB300):
-//  - One CTA per (pair of adjacent 128-row query tiles, query head,
-//    sequence), so every K/V tile loaded serves 256 query rows.  The grid's
-//    z index runs over pairs from the last (most keys under the causal mask)
-//    to the first, so the heaviest CTAs are dispatched first.
+//  - Persistent: one CTA per SM walks work items, an item being a pair of
+//    adjacent 128-row query tiles of one query head of one sequence, so
+//    every K/V tile loaded serves 256 query rows.  Items are numbered
+//    heaviest first (most keys under the causal mask).  With a work counter
+//    the TMA lane takes the next number from it (atomicAdd), so CTAs that
+//    drew light items take more of them; without one, CTA c takes items c,
+//    c + grid, ...  Either way the number is handed to the other warps
+//    through a small ring in shared memory.
 //  - Warp 8 issues TMA loads: both Q tiles once, then 128-token K and V
 //    tiles into two-deep rings (separate K and V barriers, so QK^T can start
 //    before V lands).  Every tile is stored as two 128-byte-swizzled halves
@@ -59,15 +63,8 @@ constexpr int kPrefillThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;      // S_a at kColS + 128a, O_a at kColO + 128a
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
-
-struct Barriers {
-    uint64_t q_full, q_empty;
-    uint64_t k_full[kKStages], v_full[kVStages];
-    uint64_t k_empty[kKStages], v_empty[kVStages];
-    uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles], o_empty[kQTiles];
-    uint32_t tmem_base;
-    int failed;
-};
+constexpr int kItemRing = 4;                    // item numbers in flight between the roles
+constexpr int kItemReaders = 1 + kQTiles * 4;   // the MMA warp and every softmax warp
 
 // One unit of work: a pair of 128-row query tiles of one head of one
 // sequence.  Items are numbered heaviest first (pair index descending, then
@@ -80,6 +77,17 @@ struct Item {
     int last[kQTiles];      // last key tile of query tile a (-1: tile has no rows)
     int mask_from[kQTiles]; // first key tile that can hold keys after some row
     int n_kv;               // key tiles the pair needs
+};
+
+struct Barriers {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[kKStages], v_full[kVStages];
+    uint64_t k_empty[kKStages], v_empty[kVStages];
+    uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles], o_empty[kQTiles];
+    uint64_t item_full[kItemRing], item_empty[kItemRing];
+    Item item[kItemRing];       // decoded items; n_kv < 0 = no more work
+    uint32_t tmem_base;
+    int failed;
 };
 
 // Returns false for an item with no rows; *bad is set when the sequence is
@@ -253,6 +261,20 @@ __device__ __forceinline__ void record_failure(Barriers *bars, int *err_count) {
 
 }  // namespace
 
+// Consumer side of the item ring: every lane of the calling warp waits for
+// entry n.  Returns false when the wait gave up (the pipeline failed).  The
+// entry stays valid until the warp hands it back with release_item, which
+// each reader does once it has finished the item.
+__device__ __forceinline__ bool wait_item(Barriers *bars, int n) {
+    const bool got = mbar_wait(&bars->item_full[n % kItemRing], (n / kItemRing) & 1);
+    return __all_sync(0xffffffffu, got);
+}
+
+__device__ __forceinline__ void release_item(Barriers *bars, int n, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[n % kItemRing]);
+}
+
 // kPaged: K/V tiles come from the paged cache through the block table.
 // kOffset: some sequence may have Lk > Lq (causality aligned to the last key);
 // without it every sequence has Lk == Lq and only diagonal tiles mask.
@@ -287,6 +309,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&bars->p_full[a], 4);
             mbar_init(&bars->o_full[a], 1);
             mbar_init(&bars->o_empty[a], 4);
+        }
+        for (int r = 0; r < kItemRing; ++r) {
+            mbar_init(&bars->item_full[r], 1);
+            mbar_init(&bars->item_empty[r], kItemReaders);
         }
         bars->failed = 0;
         fence_mbarrier_init();
@@ -352,13 +378,42 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 ++vcnt;
                 return true;
             };
-            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
-                Item it;
-                bool bad = false;
-                if (!decode_item(w, p, n_pairs, it, &bad)) {
+            // Items are decoded here once and published, whole, through the
+            // ring; empty items (no rows) are never published.  With a work
+            // counter the next item is drawn right after the current one's
+            // last load, so items go out in about the order CTAs free up and
+            // CTAs working on neighbouring items (the heads of one kv group,
+            // the pairs of one sequence) share K/V tiles in L2.  Drawing a
+            // whole item ahead measured slower for that reason.
+            int r = 0, n = 0;
+            auto fetch = [&](Item &it) {
+                for (;;) {
+                    const int w = p.work_counter ? atomicAdd(p.work_counter, 1)
+                                                 : (int)blockIdx.x + r * (int)gridDim.x;
+                    ++r;
+                    if (w >= n_items) {
+                        it.n_kv = -1;                       // end of work
+                        return;
+                    }
+                    bool bad = false;
+                    if (decode_item(w, p, n_pairs, it, &bad)) return;
                     if (bad) count_error(p.err_count);
-                    continue;
                 }
+            };
+            auto publish = [&](const Item &it) {
+                const int slot = n % kItemRing;
+                if (n >= kItemRing &&
+                    !mbar_wait(&bars->item_empty[slot], ((n / kItemRing) - 1) & 1))
+                    return false;
+                bars->item[slot] = it;
+                mbar_arrive(&bars->item_full[slot]);
+                ++n;
+                return true;
+            };
+            Item it;
+            fetch(it);
+            ok = publish(it);
+            while (ok && it.n_kv >= 0) {
                 const bool has1 = it.last[1] >= 0;
                 if (qcnt >= 1 && !mbar_wait(&bars->q_empty, (qcnt - 1) & 1)) {
                     ok = false;
@@ -377,6 +432,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (j + 1 < it.n_kv) ok = load_k(it, j + 1);
                     if (ok) ok = load_v(it, j);
                 }
+                if (!ok) break;
+                fetch(it);
+                ok = publish(it);
             }
             if (!ok) record_failure(bars, p.err_count);
         }
@@ -393,9 +451,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         bool ok = true;
         int qcnt = 0, kcnt = 0, vcnt = 0;        // tiles consumed so far
         int pcnt[kQTiles] = {0, 0}, ocnt[kQTiles] = {0, 0};
-        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
-            Item it;
-            if (!decode_item(w, p, n_pairs, it)) continue;
+        for (int n = 0; ok; ++n) {
+            if (!wait_item(bars, n)) {
+                ok = false;
+                break;
+            }
+            // A private copy: every field stays in registers on the issue path
+            // (a reference would be reloaded from shared memory after each wait).
+            const Item it = bars->item[n % kItemRing];
+            if (it.n_kv < 0) break;
             const bool has1 = it.last[1] >= 0;
             ok = wait_all(&bars->q_full, qcnt & 1);
             ++qcnt;
@@ -501,6 +565,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             }
             kcnt += it.n_kv;
             vcnt += it.n_kv;
+            release_item(bars, n, lane);
         }
         if (!ok && lane == 0) record_failure(bars, p.err_count);
     } else {
@@ -511,11 +576,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         const uint32_t col_s = kColS + 128 * a, col_o = kColO + 128 * a;
         bool ok = true;
         int scnt = 0, ocnt = 0;
-        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
-            Item it;
-            if (!decode_item(w, p, n_pairs, it)) continue;
+        for (int n = 0; ok; ++n) {
+            if (!wait_item(bars, n)) {
+                ok = false;
+                break;
+            }
+            const Item &it = bars->item[n % kItemRing];
+            if (it.n_kv < 0) break;
             const int last = a ? it.last[1] : it.last[0];
-            if (last < 0) continue;                       // this query tile has no rows
+            if (last < 0) {                               // this query tile has no rows
+                release_item(bars, n, lane);
+                continue;
+            }
             // kOffset: keys after a row can reach into tile mask_from = last - 1;
             // row `row` sees key c of tile j iff c <= vis_row - 128 j.  Without
             // it (Lk == Lq) only the diagonal tile masks, at c <= row.
@@ -669,6 +741,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->o_empty[a]);
+            release_item(bars, n, lane);
         }
         if (!ok) record_failure(bars, p.err_count);
     }
@@ -701,8 +774,12 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         sms = 148;
-    // Persistent: one CTA per SM, each walking items blockIdx.x, +grid, ...
+    // Persistent: one CTA per SM.  The work counter starts every launch at 0.
     const int grid = (int)(items < sms ? items : sms);
+    if (p.work_counter) {
+        const cudaError_t e = cudaMemsetAsync(p.work_counter, 0, sizeof(int), s);
+        if (e != cudaSuccess) return e;
+    }
     prefill_attn_kernel<kPaged, kOffset><<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(
         q_map, k_map, v_map, p, n_pairs, (int)items);
     return cudaGetLastError();

@@ -98,9 +98,9 @@ def test_store_kvcache_rejects_bad_arguments(lib):
 def test_prefill_rejects_bad_arguments(lib):
     f = lib.nv_prefill_attn_varlen
 
-    def call(Hq=32, Hkv=8, d=128, causal=1, q=FAKE, qs=6144, B=2, scale=0.088):
+    def call(Hq=32, Hkv=8, d=128, causal=1, q=FAKE, qs=6144, B=2, scale=0.088, sc=None):
         return f(q, qs, FAKE, 6144, FAKE, 6144, FAKE, FAKE, FAKE, B, 100, 100, 64, 64, Hq, Hkv, d,
-                 scale, causal, None, None)
+                 scale, causal, sc, None, None)
 
     assert call(Hq=30) == NV_EINVAL                  # Hq % Hkv != 0
     assert call(d=64) == NV_EUNSUPPORTED
@@ -109,6 +109,7 @@ def test_prefill_rejects_bad_arguments(lib):
     assert call(q=MIS) == NV_EALIGN
     assert call(qs=6148) == NV_EALIGN
     assert call(scale=0.0) == NV_EINVAL
+    assert call(sc=FAKE + 2) == NV_EALIGN            # work counter must be 4-byte aligned
     assert call(B=0) == NV_OK
 
 
@@ -147,9 +148,9 @@ def test_rope_table_rejects_bad_arguments(lib):
 def test_paged_prefill_rejects_bad_arguments(lib):
     f = lib.nv_prefill_attn_paged
 
-    def call(bs=256, d=128, causal=1, bt=FAKE, q=FAKE, Hq=32, Hkv=8, B=2):
+    def call(bs=256, d=128, causal=1, bt=FAKE, q=FAKE, Hq=32, Hkv=8, B=2, sc=None):
         return f(q, 4096, FAKE, FAKE, bt, 16, FAKE, FAKE, FAKE, B, 100, 64, Hq, Hkv, d, bs, 1000,
-                 0.088, causal, None, None)
+                 0.088, causal, sc, None, None)
 
     assert call(bs=192) == NV_EUNSUPPORTED          # block must hold whole 128-key tiles
     assert call(d=64) == NV_EUNSUPPORTED
@@ -157,6 +158,7 @@ def test_paged_prefill_rejects_bad_arguments(lib):
     assert call(bt=None) == NV_EINVAL
     assert call(Hq=12) == NV_EINVAL
     assert call(q=MIS) == NV_EALIGN
+    assert call(sc=FAKE + 1) == NV_EALIGN
     assert call(B=0) == NV_OK
 
 

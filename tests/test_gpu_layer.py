@@ -59,7 +59,8 @@ def test_small_layer_prefill_then_eight_decode_steps():
     cu = dev_i32(pre.cu_seqlens)
     o = torch.empty(T, s.hq, 128, dtype=torch.bfloat16, device="cuda")
     ml = int(pre.lengths.max())
-    nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, ml, ml, SCALE, err_count=err)
+    sched = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, ml, ml, SCALE, err_count=err, sched_counter=sched)
     torch.cuda.synchronize()
     check_norm(y, r, pre.x, pre.residual, "prefill")
     q_rot, k_rot = rope_ref(pre.qkv, pre.positions)

@@ -19,7 +19,13 @@ import paged_kv_attention_kvcache_gb300 as nv  # noqa: E402
 SCALE = 128 ** -0.5
 
 
-def run_prefill(qkv_bits, lengths, hq, hkv):
+def sched_counter(dynamic=True):
+    """The work counter for the dynamic schedule, deliberately left dirty: the
+    call must clear it itself.  None selects the round-robin schedule."""
+    return torch.full((1,), 987654, dtype=torch.int32, device="cuda") if dynamic else None
+
+
+def run_prefill(qkv_bits, lengths, hq, hkv, dynamic=True):
     """Prefill over views of a packed qkv buffer [T, (hq + 2 hkv) * 128]."""
     T = qkv_bits.shape[0]
     Q, D = hq * 128, hkv * 128
@@ -31,7 +37,7 @@ def run_prefill(qkv_bits, lengths, hq, hkv):
     o = torch.empty(T, hq, 128, dtype=torch.bfloat16, device="cuda")
     err = err_counter()
     nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, int(max(lengths)), int(max(lengths)), SCALE,
-                              err_count=err)
+                              err_count=err, sched_counter=sched_counter(dynamic))
     torch.cuda.synchronize()
     assert int(err.item()) == 0, "pipeline failure flagged"
     return host(o)
@@ -44,10 +50,10 @@ def split_qkv(qkv_bits, hq, hkv):
             qkv_bits[:, Q + D:].reshape(T, hkv, 128))
 
 
-def case(seed, lengths, hq, hkv, rows=None):
+def case(seed, lengths, hq, hkv, rows=None, dynamic=True):
     T = int(sum(lengths))
     qkv = wl.normal_bf16(seed, "prefill.qkv", (T, (hq + 2 * hkv) * 128))
-    got = run_prefill(qkv, lengths, hq, hkv)
+    got = run_prefill(qkv, lengths, hq, hkv, dynamic)
     q, k, v = split_qkv(qkv, hq, hkv)
     cu = wl.cu_seqlens(lengths)
     ref = oracle.attention_varlen(q, k, v, cu, cu, SCALE, True, rows=rows)
@@ -66,8 +72,25 @@ def test_prefill_exact_tiles():
 
 
 @pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (8, 2)])
-def test_prefill_ragged_packed_sequences(hq, hkv):
-    case(510 + hq, [1, 127, 128, 129, 300, 37, 2], hq, hkv)
+@pytest.mark.parametrize("dynamic", [True, False])
+def test_prefill_ragged_packed_sequences(hq, hkv, dynamic):
+    case(510 + hq, [1, 127, 128, 129, 300, 37, 2], hq, hkv, dynamic=dynamic)
+
+
+def test_prefill_more_items_than_ctas_both_schedules_agree():
+    # 40 sequences x 8 heads of up to 1000 tokens: several items per CTA under
+    # either schedule; both must give the oracle's result.
+    g = np.random.default_rng(515)
+    lengths = g.integers(1, 1000, 40)
+    T = int(lengths.sum())
+    qkv = wl.normal_bf16(515, "prefill.qkv", (T, (8 + 2 * 2) * 128))
+    rows = np.stack([g.integers(0, T, 800), g.integers(0, 8, 800)], axis=1).astype(np.int64)
+    q, k, v = split_qkv(qkv, 8, 2)
+    cu = wl.cu_seqlens(lengths)
+    ref = oracle.attention_varlen(q, k, v, cu, cu, SCALE, True, rows=rows)
+    for dynamic in (True, False):
+        got = run_prefill(qkv, lengths, 8, 2, dynamic)
+        check_close(got[rows[:, 0], rows[:, 1]], ref, f"prefill many items dynamic={dynamic}")
 
 
 def test_prefill_small_layer_shape():
@@ -111,14 +134,15 @@ def test_prefill_contiguous_keys_with_prefix():
     o = torch.empty(int(new.sum()), hq, 128, dtype=torch.bfloat16, device="cuda")
     err = err_counter()
     nv.nv_prefill_attn_varlen(dev(q), dev(k), dev(v), o, dev_i32(cu_q), dev_i32(cu_k),
-                              int(new.max()), int(lk.max()), SCALE, err_count=err)
+                              int(new.max()), int(lk.max()), SCALE, err_count=err,
+                              sched_counter=sched_counter())
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     ref = oracle.attention_varlen(q, k, v, cu_q, cu_k, SCALE, True)
     check_close(host(o), ref, "prefill with contiguous prefix")
 
 
-def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3):
+def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3, dynamic=True):
     g = np.random.default_rng(seed)
     prefix, new = np.asarray(prefix), np.asarray(new)
     lk = prefix + new
@@ -138,7 +162,8 @@ def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3):
     o = torch.empty(int(new.sum()), hq, 128, dtype=torch.bfloat16, device="cuda")
     err = err_counter()
     nv.nv_prefill_attn_paged(dev(q), dev(kc), dev(vc), dev_i32(bt), o, dev_i32(cu_q),
-                             dev_i32(cu_k), int(new.max()), SCALE, err_count=err)
+                             dev_i32(cu_k), int(new.max()), SCALE, err_count=err,
+                             sched_counter=sched_counter(dynamic))
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     ref = oracle.attention_paged_prefill(q, kc, vc, bt, cu_q, cu_k, SCALE, rows=rows)
@@ -159,6 +184,12 @@ def test_prefill_paged_equals_contiguous_when_no_prefix():
     # With no cached prefix the paged path must agree with the contiguous one.
     got, ref = _paged_case(550, prefix=[0, 0, 0], new=[37, 300, 128], hq=16, hkv=8)
     check_close(got, ref, "paged prefill, no prefix")
+
+
+def test_prefill_paged_round_robin_schedule():
+    got, ref = _paged_case(551, prefix=[0, 37, 256, 300, 511, 1000],
+                           new=[5, 1, 128, 200, 129, 300], hq=8, hkv=2, dynamic=False)
+    check_close(got, ref, "paged prefill, round-robin")
 
 
 def test_prefill_paged_chunked_qwen3_8b_sampled():
