@@ -302,35 +302,55 @@ def run_ours(args, rank, world, local_rank):
     pflops = prefill_flops(pre.lengths)
     ptflops = pflops / (pattn_sum / args.steps / 1e3) / 1e12
 
-    # ---- e2e: host buffers through the C-ABI, copies inside the timed region
-    pinned = {
-        "x": torch.from_numpy(step.x.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "r": torch.from_numpy(step.residual.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "qkv": torch.from_numpy(step.qkv.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "pos": torch.from_numpy(step.positions).pin_memory(),
-        "slots": torch.from_numpy(step.slot_mapping).pin_memory(),
-        "bt": torch.from_numpy(step.block_tables).pin_memory(),
-        "ctx": torch.from_numpy(step.context_lens).pin_memory(),
-    }
-    outs = {"y": torch.empty(B, H, dtype=torch.bfloat16).pin_memory(),
-            "r": torch.empty(B, H, dtype=torch.bfloat16).pin_memory(),
-            "o": torch.empty(B, s.hq, 128, dtype=torch.bfloat16).pin_memory()}
-    devs = {k: torch.empty_like(v, device=dev_t) for k, v in pinned.items()}
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    # ---- e2e: host buffers through the C-ABI, copies inside the timed region.
+    # The step's inputs sit in one pinned buffer and go over in one copy; the
+    # normed hidden state and the new residual come back on a side stream as
+    # soon as add-RMSNorm has written them (overlapping the attention), the
+    # attention output after the decode kernel.
+    MB = step.block_tables.shape[1]
+    in_specs = [("x", step.x.view(np.int16), torch.bfloat16),
+                ("r", step.residual.view(np.int16), torch.bfloat16),
+                ("qkv", step.qkv.view(np.int16), torch.bfloat16),
+                ("pos", step.positions, torch.int64),
+                ("slots", step.slot_mapping, torch.int32),
+                ("bt", step.block_tables, torch.int32),
+                ("ctx", step.context_lens, torch.int32)]
+    offs, off = {}, 0
+    for name, arr, _ in in_specs:
+        offs[name] = off
+        off += (arr.nbytes + 255) // 256 * 256
+    host_in = torch.zeros(off, dtype=torch.uint8).pin_memory()
+    for name, arr, _ in in_specs:
+        host_in[offs[name]:offs[name] + arr.nbytes].copy_(
+            torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
+    dev_in = torch.empty(off, dtype=torch.uint8, device=dev_t)
+    dv = {name: dev_in[offs[name]:offs[name] + arr.nbytes].view(dt).view(arr.shape)
+          for name, arr, dt in in_specs}
+    dev_out = torch.empty(2, B, H, dtype=torch.bfloat16, device=dev_t)     # y, new residual
+    host_yr = torch.empty(2, B, H, dtype=torch.bfloat16).pin_memory()
+    host_o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(arr.nbytes for _, arr, _ in in_specs)
+    d2h = host_yr.numel() * 2 + host_o.numel() * 2
+    side = torch.cuda.Stream(device=dev_t)
+    q2, k2, v2 = decode_views(dv["qkv"])
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
-        e0, e1 = ev(), ev()
+        e0, e1, ev_norm, ev_side = ev(), ev(), ev(), ev()
         e0.record()
-        for k_, v_ in pinned.items():
-            devs[k_].copy_(v_, non_blocking=True)
-        q2, k2, v2 = decode_views(devs["qkv"])
-        decode_layer(x=devs["x"], r=devs["r"], y=d_y, q=q2, k=k2, v=v2, pos=devs["pos"],
-                     slots=devs["slots"], bt=devs["bt"], ctx=devs["ctx"], o=d_o)
-        outs["y"].copy_(d_y, non_blocking=True)
-        outs["r"].copy_(devs["r"], non_blocking=True)
-        outs["o"].copy_(d_o, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
+        nv.nv_add_rmsnorm(dv["x"], dv["r"], d_g, dev_out[0], dev_out[1], eps=wl.RMS_EPS)
+        ev_norm.record()
+        side.wait_event(ev_norm)
+        with torch.cuda.stream(side):
+            host_yr.copy_(dev_out, non_blocking=True)
+            ev_side.record(side)
+        nv.nv_qknorm_rope(q2, k2, d_qn, d_kn, table, dv["pos"], eps=wl.RMS_EPS, err_count=err)
+        nv.nv_store_kvcache(k2, v2, kc, vc, dv["slots"], err)
+        nv.nv_decode_attn_paged(q2, kc, vc, dv["bt"], dv["ctx"], d_o, SCALE, workspace=ws,
+                                err_count=err)
+        host_o.copy_(d_o, non_blocking=True)
+        torch.cuda.current_stream().wait_event(ev_side)
         e1.record()
         torch.cuda.synchronize()
         if i >= args.warmup:
