@@ -154,3 +154,12 @@ def test_decode_qwen3_8b_batch256_full_size():
 def test_decode_long_context_split_kv_full_size(split):
     step = wl.config5()
     _full_config(step, 96, 405, split=split)
+
+
+def test_decode_longest_context():
+    # Contexts of the longest length the model takes, next to a single key.
+    ctx = [wl.MAX_POSITION, 1, wl.MAX_POSITION - 1]
+    q, k, v, bt, ctx = random_case(306, len(ctx), 32, 8, ctx)
+    got, err = run_decode(q, k, v, bt, ctx)
+    assert err == 0
+    check_close(got, oracle.paged_decode(q, k, v, bt, ctx, SCALE), "decode 40960")

@@ -203,3 +203,18 @@ def test_prefill_paged_chunked_qwen3_8b_sampled():
     rows = np.stack([toks, g.integers(0, 32, toks.size)], axis=1).astype(np.int64)
     got, ref = _paged_case(561, prefix, new, 32, 8, rows=rows)
     check_close(got, ref, "chunked prefill 8b")
+
+
+def test_prefill_longest_context_single_sequence_sampled():
+    # One sequence of the longest context the model takes (40960 tokens) at
+    # Qwen3-8B heads: 160 query-tile pairs, the heaviest item 320 key tiles.
+    L, hq, hkv = wl.MAX_POSITION, 32, 8
+    qkv = wl.normal_bf16(570, "prefill.max", (L, (hq + 2 * hkv) * 128))
+    g = np.random.default_rng(571)
+    toks = np.concatenate([[0, 127, 128, 255, 256, L - 129, L - 128, L - 1], g.integers(0, L, 56)])
+    rows = np.stack([toks, g.integers(0, hq, toks.size)], axis=1).astype(np.int64)
+    got = run_prefill(qkv, [L], hq, hkv)
+    q, k, v = split_qkv(qkv, hq, hkv)
+    cu = wl.cu_seqlens([L])
+    ref = oracle.attention_varlen(q, k, v, cu, cu, SCALE, True, rows=rows)
+    check_close(got[rows[:, 0], rows[:, 1]], ref, "prefill 40960 sampled")
