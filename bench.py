@@ -46,6 +46,10 @@ SCALE = 128 ** -0.5
 # decode_split_kernel over its algorithmic bytes), valid only for the kernel
 # source it was taken on.
 DECODE_TRAFFIC = {"ratio": 1.0062, "source_sha256_16": "88592f0223f86772"}
+# DRAM bytes (read + write) of one prefill-attention launch on the bench batch
+# (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
+# of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
+PREFILL_TRAFFIC = {"bytes": 1145854080, "source_sha256_16": "287cf849927b38bc"}
 
 
 def kernel_source_hash(name: str) -> str:
@@ -599,6 +603,54 @@ def run_ncu_case(which: str, launches: int = 3):
     print(f"ncu case {which}: {launches} launches done")
 
 
+def run_ncu_layer_case(launches: int = 2):
+    """Every kernel of the Qwen3-8B prefill layer on the bench batch (33,109
+    tokens), plus the fused rope+store pass and SiluAndMul (I = 12288), each
+    `launches` times: ~3 GB on the device, inputs above L2 size."""
+    import torch
+    import __graft_entry__
+    import paged_kv_attention_kvcache_gb300 as nv
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).cuda()
+
+    pre = wl.config4()
+    s = pre.shape
+    T, Q, D = pre.qkv.shape[0], s.q_size, s.kv_size
+    table = torch.empty(wl.MAX_POSITION, 128, dtype=torch.float32, device="cuda")
+    nv.nv_rope_cos_sin_cache(table, wl.ROPE_BASE)
+    x, r, g = dev(pre.x), dev(pre.residual), dev(pre.gamma)
+    y = torch.empty_like(x)
+    qkv = dev(pre.qkv)
+    q, k, v = (qkv[:, :Q].view(T, s.hq, 128), qkv[:, Q:Q + D].view(T, s.hkv, 128),
+               qkv[:, Q + D:].view(T, s.hkv, 128))
+    qn, kn = dev(pre.q_norm_w), dev(pre.k_norm_w)
+    pos = torch.from_numpy(pre.positions).cuda()
+    slots = torch.from_numpy(pre.slot_mapping).cuda()
+    cu = torch.from_numpy(pre.cu_seqlens).cuda()
+    kc = torch.zeros(pre.num_blocks, wl.BLOCK_SIZE, s.hkv, 128, dtype=torch.bfloat16,
+                     device="cuda")
+    vc = torch.zeros_like(kc)
+    o = torch.empty(T, s.hq, 128, dtype=torch.bfloat16, device="cuda")
+    sched = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ml = int(pre.lengths.max())
+    gate_up = torch.empty(T, 2 * 12288, dtype=torch.bfloat16, device="cuda").normal_()
+    act = torch.empty(T, 12288, dtype=torch.bfloat16, device="cuda")
+    for _ in range(launches):
+        nv.nv_add_rmsnorm(x, r, g, y, r, eps=wl.RMS_EPS)
+        nv.nv_qknorm_rope(q, k, qn, kn, table, pos, eps=wl.RMS_EPS)
+        nv.nv_store_kvcache(k, v, kc, vc, slots)
+        nv.nv_prefill_attn_varlen(q, k, v, o, cu, cu, ml, ml, SCALE, sched_counter=sched)
+        nv.nv_qknorm_rope_store(q, k, v, qn, kn, table, pos, kc, vc, slots, eps=wl.RMS_EPS,
+                                write_k=True)
+        nv.nv_silu_and_mul(gate_up, act)
+    torch.cuda.synchronize()
+    print(f"ncu case layer: {launches} launches of each kernel done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,9 +658,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None,
-                    help="run a small case of one kernel (for ncu captures) and exit")
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "layer"], default=None,
+                    help="run a small case of one kernel, or every prefill-layer kernel on the "
+                         "bench batch (for ncu captures), and exit")
     args = ap.parse_args()
+    if args.ncu_case == "layer":
+        run_ncu_layer_case()
+        return
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
         return
@@ -665,7 +721,11 @@ def main():
                         "unit": "TFLOP/s", "launch_ms": r["pattn_ms"],
                         "roofline": {"bound": "tensor", "achieved": r["ptflops"],
                                      "peak": r["bf16"], "unit": "TFLOP/s",
-                                     "frac": r["ptflops"] / r["bf16"], "traffic": None,
+                                     "frac": r["ptflops"] / r["bf16"],
+                                     "traffic": (PREFILL_TRAFFIC["bytes"]
+                                                 if kernel_source_hash("prefill_attn.cu")
+                                                 == PREFILL_TRAFFIC["source_sha256_16"] else None),
+                                     "traffic_unit": "bytes per launch",
                                      "peak_source": r["peak_src"] + " bf16 burst"}},
             "cpu_baseline": cpu,
             "e2e": {"value": r["e2e"], "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
