@@ -41,8 +41,8 @@ METRIC = "paged-attn decode HBM GB/s (% peak); prefill attn TFLOP/s, Qwen3-8B sh
 SCALE = 128 ** -0.5
 
 
-# DRAM bytes per algorithmic byte of the decode attention kernels, from the
-# ncu capture in profiles/decode_attn_qwen3_8b_64x4096.md (reads + writes of
+# DRAM bytes per algorithmic byte of the decode attention kernels, from an
+# ncu capture of `bench.py --ncu-case decode` (reads + writes of
 # decode_split_kernel over its algorithmic bytes), valid only for the kernel
 # source it was taken on.
 DECODE_TRAFFIC = {"ratio": 1.0062, "source_sha256_16": "88592f0223f86772"}
@@ -50,6 +50,25 @@ DECODE_TRAFFIC = {"ratio": 1.0062, "source_sha256_16": "88592f0223f86772"}
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
 PREFILL_TRAFFIC = {"bytes": 1145854080, "source_sha256_16": "287cf849927b38bc"}
+
+
+def max_over_ranks(values, world: int, device=None):
+    """Each timing's maximum over all ranks: the slowest replica sets the
+    job's time.  With one rank the values come back unchanged."""
+    values = [float(v) for v in values]
+    if world <= 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest
+    rank's time (replicas each do the same work)."""
+    return world * units_per_rank / seconds
 
 
 def kernel_source_hash(name: str) -> str:
@@ -289,18 +308,12 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [a + b for a, b in zip(dec_ms, pre_ms)]
     assert int(err.item()) == 0, f"device error count {int(err.item())}"
 
-    dec_time = sum(dec_ms) / 1e3
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([dec_time, tot_ms, sum(pattn_ms)], dtype=torch.float64, device=dev_t)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_time, tot_ms, pattn_sum = t.tolist()
-    else:
-        pattn_sum = sum(pattn_ms)
+    dec_time, tot_ms, pattn_sum = max_over_ranks(
+        [sum(dec_ms) / 1e3, sum(step_ms), sum(pattn_ms)], world, dev_t)
 
     nbytes = decode_step_bytes(step)
     hbm, bf16, bf16_sus, peak_src = measured_peaks()
-    value = world * nbytes["total"] * args.steps / dec_time / 1e9
+    value = job_throughput(nbytes["total"] * args.steps, world, dec_time) / 1e9
     attn_avg_s = statistics.mean(attn_ms) / 1e3
     attn_gbs = nbytes["attn"] / attn_avg_s / 1e9
     pflops = prefill_flops(pre.lengths)
@@ -359,7 +372,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_val = world * nbytes["total"] / (statistics.mean(e2e_ms) / 1e3) / 1e9
+    e2e_s = max_over_ranks([statistics.mean(e2e_ms) / 1e3], world, dev_t)[0]
+    e2e_val = job_throughput(nbytes["total"], world, e2e_s) / 1e9
 
     graph_info = graph_decode_overhead(dev_t)
 
