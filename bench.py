@@ -45,11 +45,11 @@ SCALE = 128 ** -0.5
 # ncu capture of `bench.py --ncu-case decode` (reads + writes of
 # decode_split_kernel over its algorithmic bytes), valid only for the kernel
 # source it was taken on.
-DECODE_TRAFFIC = {"ratio": 1.0062, "source_sha256_16": "88592f0223f86772"}
+DECODE_TRAFFIC = {"ratio": 1.0037, "source_sha256_16": "6069696183c8d8aa"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1145854080, "source_sha256_16": "287cf849927b38bc"}
+PREFILL_TRAFFIC = {"bytes": 1144340608, "source_sha256_16": "a5c69de502c1b120"}
 
 
 def max_over_ranks(values, world: int, device=None):

@@ -24,6 +24,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// so that it may be scheduled while the previous kernel in the stream drains,
+// and starts with this: wait until that kernel has completed and its writes
+// are visible (a no-op without such a predecessor), then allow the next
+// kernel's CTAs to be scheduled.  The runtime schedules those only once every
+// CTA of this grid has got here, so they never take resources this grid
+// still needs; memory ordering is exactly that of plain launches.
+__device__ __forceinline__ void pdl_wait_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void count_error(int *err_count, int n = 1) {
     if (err_count) atomicAdd(err_count, n);
 }

@@ -54,6 +54,7 @@ __device__ __forceinline__ void named_barrier_consumers() {
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
+    pdl_wait_release();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.Hq / p.Hkv;
@@ -314,6 +315,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 // One warp per (sequence, query head): combine the splits' partial outputs.
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const DecodeParams p) {
+    pdl_wait_release();
     const int64_t wid = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)p.B * p.Hq) return;
@@ -385,12 +387,12 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &k_map,
     }
     if (p.B == 0) return cudaSuccess;
     dim3 grid(p.max_splits, p.Hkv, p.B);
-    decode_split_kernel<<<grid, kDecodeThreads, kDecodeSmemBytes, s>>>(k_map, v_map, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_split_kernel, grid, dim3(kDecodeThreads),
+                               (size_t)kDecodeSmemBytes, s, k_map, v_map, p);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     const int64_t warps = (int64_t)p.B * p.Hq;
-    decode_merge_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(decode_merge_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256),
+                      (size_t)0, s, p);
 }
 
 }  // namespace nvattn

@@ -13,6 +13,7 @@ namespace nvattn {
 // formed in fp64 so that only the final value is rounded to fp32.
 __global__ void rope_cos_sin_kernel(float *__restrict__ cos_sin, int max_position,
                                     int rotary_dim, double base) {
+    pdl_wait_release();
     const int half = rotary_dim / 2;
     const int64_t n = (int64_t)max_position * half;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
@@ -35,9 +36,8 @@ cudaError_t launch_rope_cos_sin(float *cos_sin, int max_position, int rotary_dim
     const int threads = 256;
     int64_t blocks = (n + threads - 1) / threads;
     if (blocks > 4096) blocks = 4096;
-    rope_cos_sin_kernel<<<(unsigned)blocks, threads, 0, s>>>(cos_sin, max_position, rotary_dim,
-                                                              base);
-    return cudaGetLastError();
+    return launch_pdl(rope_cos_sin_kernel, dim3((unsigned)blocks), dim3(threads), (size_t)0, s,
+                      cos_sin, max_position, rotary_dim, base);
 }
 
 // --------------------------------------------------------- add + RMSNorm
@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kNormThreads)
 add_rmsnorm_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ residual,
                    const uint4 *__restrict__ weight, uint4 *__restrict__ out,
                    uint4 *__restrict__ residual_out, int nvec, float inv_h, float eps) {
+    pdl_wait_release();
     const int64_t row = blockIdx.x;
     const uint4 *xr = x + row * nvec;
     float s[VPT][8];
@@ -117,14 +118,12 @@ static cudaError_t launch_norm_vpt(const uint16_t *x, const uint16_t *residual,
     const float inv_h = 1.0f / (float)H;
     dim3 grid((unsigned)T);
     if (residual)
-        add_rmsnorm_kernel<VPT, true><<<grid, kNormThreads, 0, s>>>(
-            (const uint4 *)x, (const uint4 *)residual, (const uint4 *)weight, (uint4 *)out,
-            (uint4 *)residual_out, nvec, inv_h, eps);
-    else
-        add_rmsnorm_kernel<VPT, false><<<grid, kNormThreads, 0, s>>>(
-            (const uint4 *)x, nullptr, (const uint4 *)weight, (uint4 *)out, nullptr, nvec,
-            inv_h, eps);
-    return cudaGetLastError();
+        return launch_pdl(add_rmsnorm_kernel<VPT, true>, grid, dim3(kNormThreads), (size_t)0, s,
+                          (const uint4 *)x, (const uint4 *)residual, (const uint4 *)weight,
+                          (uint4 *)out, (uint4 *)residual_out, nvec, inv_h, eps);
+    return launch_pdl(add_rmsnorm_kernel<VPT, false>, grid, dim3(kNormThreads), (size_t)0, s,
+                      (const uint4 *)x, (const uint4 *)nullptr, (const uint4 *)weight,
+                      (uint4 *)out, (uint4 *)nullptr, nvec, inv_h, eps);
 }
 
 cudaError_t launch_add_rmsnorm(const uint16_t *x, const uint16_t *residual,
@@ -214,6 +213,7 @@ qknorm_rope_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restr
                    const uint16_t *__restrict__ kw, const float *__restrict__ cos_sin,
                    int max_position, const int64_t *__restrict__ positions, int64_t T, int Hq,
                    int Hkv, float eps, int *err_count) {
+    pdl_wait_release();
     const int heads = Hq + Hkv;
     const int64_t n_rows = T * heads;
     const int lane = threadIdx.x & 31;
@@ -253,10 +253,9 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
     const unsigned blocks = (unsigned)((threads + kRopeThreads - 1) / kRopeThreads);
-    qknorm_rope_kernel<<<blocks, kRopeThreads, 0, s>>>(q, q_stride, k, k_stride, qw, kw, cos_sin,
-                                                       max_position, positions, T, Hq, Hkv, eps,
-                                                       err_count);
-    return cudaGetLastError();
+    return launch_pdl(qknorm_rope_kernel, dim3(blocks), dim3(kRopeThreads), (size_t)0, s, q,
+                      q_stride, k, k_stride, qw, kw, cos_sin, max_position, positions, T, Hq, Hkv,
+                      eps, err_count);
 }
 
 // ------------------------------------------ QK-Norm + RoPE + store_kvcache
@@ -277,6 +276,7 @@ qknorm_rope_store_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *_
                          const int32_t *__restrict__ slot_mapping, uint16_t *__restrict__ k_cache,
                          uint16_t *__restrict__ v_cache, int64_t num_slots, int64_t T, int Hq,
                          int Hkv, float eps, int write_k, int *err_count) {
+    pdl_wait_release();
     const int heads = Hq + 2 * Hkv;
     const int64_t n_rows = T * heads;
     const int lane = threadIdx.x & 31;
@@ -339,10 +339,10 @@ cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
     const unsigned blocks = (unsigned)((threads + kRopeThreads - 1) / kRopeThreads);
-    qknorm_rope_store_kernel<<<blocks, kRopeThreads, 0, s>>>(
-        q, q_stride, k, k_stride, v, v_stride, qw, kw, cos_sin, max_position, positions,
-        slot_mapping, k_cache, v_cache, num_slots, T, Hq, Hkv, eps, write_k, err_count);
-    return cudaGetLastError();
+    return launch_pdl(qknorm_rope_store_kernel, dim3(blocks), dim3(kRopeThreads), (size_t)0, s, q,
+                      q_stride, k, k_stride, v, v_stride, qw, kw, cos_sin, max_position,
+                      positions, slot_mapping, k_cache, v_cache, num_slots, T, Hq, Hkv, eps,
+                      write_k, err_count);
 }
 
 }  // namespace nvattn

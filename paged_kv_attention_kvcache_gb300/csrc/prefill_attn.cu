@@ -284,6 +284,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const PrefillParams p,
                     int n_pairs, int n_items) {
+    pdl_wait_release();
     if (pipeline_failed_before(p.err_count)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float sl2 = p.scale_log2;
@@ -780,9 +781,8 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q
         const cudaError_t e = cudaMemsetAsync(p.work_counter, 0, sizeof(int), s);
         if (e != cudaSuccess) return e;
     }
-    prefill_attn_kernel<kPaged, kOffset><<<grid, kPrefillThreads, kPrefillSmemBytes, s>>>(
-        q_map, k_map, v_map, p, n_pairs, (int)items);
-    return cudaGetLastError();
+    return launch_pdl(prefill_attn_kernel<kPaged, kOffset>, dim3(grid), dim3(kPrefillThreads),
+                      (size_t)kPrefillSmemBytes, s, q_map, k_map, v_map, p, n_pairs, (int)items);
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,

@@ -17,6 +17,7 @@ store_kvcache_kernel(const uint4 *__restrict__ key, int64_t key_stride_v,
                      uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                      const int32_t *__restrict__ slot_mapping, int64_t N, int vec_per_row,
                      int64_t num_slots, int *err_count) {
+    pdl_wait_release();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kStoreThreads / 32);
     for (int64_t n = ((int64_t)blockIdx.x * kStoreThreads + threadIdx.x) >> 5; n < N;
@@ -57,10 +58,10 @@ cudaError_t launch_store_kvcache(const uint16_t *key, int64_t key_stride, const 
     const int warps_per_block = kStoreThreads / 32;
     int64_t blocks = (N + warps_per_block - 1) / warps_per_block;
     if (blocks > 152 * 32) blocks = 152 * 32;
-    store_kvcache_kernel<<<(unsigned)blocks, kStoreThreads, 0, s>>>(
-        (const uint4 *)key, key_stride / 8, (const uint4 *)value, value_stride / 8,
-        (uint4 *)k_cache, (uint4 *)v_cache, slot_mapping, N, D / 8, num_slots, err_count);
-    return cudaGetLastError();
+    return launch_pdl(store_kvcache_kernel, dim3((unsigned)blocks), dim3(kStoreThreads), (size_t)0,
+                      s, (const uint4 *)key, key_stride / 8, (const uint4 *)value,
+                      value_stride / 8, (uint4 *)k_cache, (uint4 *)v_cache, slot_mapping, N,
+                      D / 8, num_slots, err_count);
 }
 
 }  // namespace nvattn

@@ -25,6 +25,7 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 __global__ void __launch_bounds__(kSwigluThreads)
 silu_and_mul_kernel(const uint4 *x, int64_t x_stride_v, uint4 *out, int64_t out_stride_v,
                     int64_t T, int nvec) {
+    pdl_wait_release();
     const int64_t total = T * nvec;
     const int64_t stride = (int64_t)gridDim.x * kSwigluThreads;
     for (int64_t base = (int64_t)blockIdx.x * kSwigluThreads + threadIdx.x; base < total;
@@ -67,9 +68,8 @@ cudaError_t launch_silu_and_mul(const uint16_t *x, int64_t x_stride, uint16_t *o
     int64_t blocks = (total + per_block - 1) / per_block;
     const int64_t wave = (int64_t)kNumSms * kSwigluBlocksPerSm;
     if (blocks > wave) blocks = wave;
-    silu_and_mul_kernel<<<(unsigned)blocks, kSwigluThreads, 0, s>>>(
-        (const uint4 *)x, x_stride / 8, (uint4 *)out, out_stride / 8, T, nvec);
-    return cudaGetLastError();
+    return launch_pdl(silu_and_mul_kernel, dim3((unsigned)blocks), dim3(kSwigluThreads), (size_t)0,
+                      s, (const uint4 *)x, x_stride / 8, (uint4 *)out, out_stride / 8, T, nvec);
 }
 
 }  // namespace nvattn
