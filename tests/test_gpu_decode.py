@@ -163,3 +163,15 @@ def test_decode_longest_context():
     got, err = run_decode(q, k, v, bt, ctx)
     assert err == 0
     check_close(got, oracle.paged_decode(q, k, v, bt, ctx, SCALE), "decode 40960")
+
+
+@pytest.mark.parametrize("bs", [64, 128, 512])
+@pytest.mark.parametrize("split", [0, 192])
+def test_decode_other_block_sizes(bs, split):
+    # Block sizes other than the pages' 256 (any multiple of the 64-key tile);
+    # a split of 192 keys straddles block boundaries for every one of them.
+    ctx = [1, bs - 1, bs, bs + 1, 3 * bs + 17, 1000]
+    q, k, v, bt, ctx = random_case(310 + bs + split, len(ctx), 16, 4, ctx, bs=bs)
+    got, err = run_decode(q, k, v, bt, ctx, split=split)
+    assert err == 0
+    check_close(got, oracle.paged_decode(q, k, v, bt, ctx, SCALE), f"decode bs={bs} split={split}")

@@ -142,13 +142,13 @@ def test_prefill_contiguous_keys_with_prefix():
     check_close(host(o), ref, "prefill with contiguous prefix")
 
 
-def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3, dynamic=True):
+def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3, dynamic=True,
+                bs=wl.BLOCK_SIZE):
     g = np.random.default_rng(seed)
     prefix, new = np.asarray(prefix), np.asarray(new)
     lk = prefix + new
-    bs = wl.BLOCK_SIZE
     nb = int(sum(math.ceil(int(x) / bs) for x in lk)) + spare
-    bt = wl.carve_block_tables(g.permutation(nb).astype(np.int32), lk)
+    bt = wl.carve_block_tables(g.permutation(nb).astype(np.int32), lk, block_size=bs)
     kc = wl.f32_to_bf16_bits(g.standard_normal((nb, bs, hkv, 128)).astype(np.float32))
     vc = wl.f32_to_bf16_bits(g.standard_normal((nb, bs, hkv, 128)).astype(np.float32))
     if nan_tail:
@@ -218,3 +218,12 @@ def test_prefill_longest_context_single_sequence_sampled():
     cu = wl.cu_seqlens([L])
     ref = oracle.attention_varlen(q, k, v, cu, cu, SCALE, True, rows=rows)
     check_close(got[rows[:, 0], rows[:, 1]], ref, "prefill 40960 sampled")
+
+
+@pytest.mark.parametrize("bs", [128, 512])
+def test_prefill_paged_other_block_sizes(bs):
+    # Block sizes other than 256 (any multiple of the 128-key tile): tiles
+    # then start at every block (128) or every fourth tile starts one (512).
+    got, ref = _paged_case(580 + bs, prefix=[0, 37, 256, 300, 640], new=[5, 130, 128, 200, 300],
+                           hq=8, hkv=2, bs=bs)
+    check_close(got, ref, f"paged prefill bs={bs}")
