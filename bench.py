@@ -376,6 +376,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_val = job_throughput(nbytes["total"], world, e2e_s) / 1e9
 
     graph_info = graph_decode_overhead(dev_t)
+    decode_sets = decode_attention_configs(dev_t)
 
     # ---- QK-Norm + RoPE + store on the prefill batch: two kernels vs one pass
     def time_us(fn, reps=20):
@@ -419,13 +420,63 @@ def run_ours(args, rank, world, local_rank):
     del gate_up, act
 
     return dict(
-        graph=graph_info, rope_store=rope_store, swiglu=swiglu,
+        graph=graph_info, rope_store=rope_store, swiglu=swiglu, decode_sets=decode_sets,
         value=value, ms_per_step=tot_ms / args.steps, dec_ms=statistics.mean(dec_ms),
         pre_ms=statistics.mean(pre_ms), attn_ms=statistics.mean(attn_ms),
         attn_gbs=attn_gbs, ptflops=ptflops, pattn_ms=pattn_sum / args.steps, clocks=clk,
         hbm=hbm, bf16=bf16, bf16_sus=bf16_sus, peak_src=peak_src, nbytes=nbytes,
         launches=launches_per_step * args.steps, e2e=e2e_val, h2d=h2d, d2h=d2h, wall=wall,
         gen_s=gen_s, step=step, pre=pre, ws_bytes=ws_bytes, T=T)
+
+
+# ------------------------------------ decode attention on the other decode sets
+def decode_attention_configs(dev_t, reps: int = 20):
+    """Paged decode attention alone on the two other decode workloads: Qwen3-0.6B
+    heads, B=64, ctx U[512, 4096] (0.6 GB of K/V), and Qwen3-8B heads, B=32, ctx
+    log-uniform in [4096, 40960] with 1% outlier K rows (2.1 GB), with the
+    automatic split and a forced 1024-key split.  L2 flushed before each rep;
+    median of `reps` event-timed launches."""
+    import torch
+    import paged_kv_attention_kvcache_gb300 as nv
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev_t)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).to(dev_t)
+
+    out = {}
+    for name, step, splits in (("b64_ctx512_4096_qwen3_06b", wl.config2(), (0,)),
+                               ("b32_ctx4096_40960_qwen3_8b", wl.config5(), (0, 1024))):
+        s = step.shape
+        B = step.context_lens.size
+        q = dev(step.qkv[:, :s.q_size]).view(B, s.hq, 128)
+        kc, vc = dev(step.pool.k), dev(step.pool.v)
+        bt = torch.from_numpy(step.block_tables).to(dev_t)
+        cl = torch.from_numpy(step.context_lens).to(dev_t)
+        o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
+        nbytes = decode_step_bytes(step)["attn"]
+        for split in splits:
+            wsb = nv.nv_decode_attn_workspace_size(B, s.hq, s.hkv, 128, bt.shape[1],
+                                                   wl.BLOCK_SIZE, split)
+            ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
+            times = []
+            for i in range(reps + 3):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws,
+                                        kv_split_tokens=split)
+                e1.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1) / 1e3)
+            t = statistics.median(times)
+            out[f"{name}_split{split or 'auto'}"] = {"kv_bytes": nbytes, "ms": t * 1e3,
+                                                      "gbs": nbytes / t / 1e9}
+        del kc, vc
+    del flush
+    return out
 
 
 # ------------------------------------------ launch overhead: CUDA graph
@@ -710,6 +761,7 @@ def main():
                          f"paged decode) repeated {reps}x, {secs:.1f} s of CPU time"}
     if rank == 0:
         nbytes = r["nbytes"]
+        B_dec = r["step"].context_lens.size
         traffic = None
         if kernel_source_hash("decode_attn.cu") == DECODE_TRAFFIC["source_sha256_16"]:
             traffic = DECODE_TRAFFIC["ratio"] * nbytes["attn"]
@@ -744,6 +796,11 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": r["e2e"], "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]},
+            "tokens_per_s": {"decode": world * B_dec / (r["dec_ms"] / 1e3),
+                             "prefill": world * r["T"] / (r["pre_ms"] / 1e3)},
+            "nominal_frac": {"decode_attn_of_7900_GBs": r["attn_gbs"] / 7900.0,
+                             "prefill_of_2250_TFLOPs": r["ptflops"] / 2250.0},
+            "decode_attention_sets": r["decode_sets"],
             "decode_graph": r["graph"],
             "rope_store_prefill": r["rope_store"],
             "silu_and_mul_prefill": r["swiglu"],
