@@ -319,15 +319,16 @@ def run_ours(args, rank, world, local_rank):
     pflops = prefill_flops(pre.lengths)
     ptflops = pflops / (pattn_sum / args.steps / 1e3) / 1e12
 
-    # ---- e2e: host buffers through the C-ABI, copies inside the timed region.
-    # The step's inputs sit in one pinned buffer and go over in one copy; the
-    # normed hidden state and the new residual come back on a side stream as
-    # soon as add-RMSNorm has written them (overlapping the attention), the
-    # attention output after the decode kernel.
+    # ---- e2e: host buffers through the C-ABI, host<->device traffic inside the
+    # timed region.  add-RMSNorm reads x and the residual straight from pinned
+    # host memory and writes y and the new residual straight back (the ABI
+    # takes device-addressable host pointers for tensors its kernels touch with
+    # plain loads and stores); qkv and the metadata go over in one packed
+    # copy (the rotation works in place, and the host inputs must stay as they
+    # are for the next step); the decode kernel writes o to pinned host memory.
+    # One stream, in the layer's order.
     MB = step.block_tables.shape[1]
-    in_specs = [("x", step.x.view(np.int16), torch.bfloat16),
-                ("r", step.residual.view(np.int16), torch.bfloat16),
-                ("qkv", step.qkv.view(np.int16), torch.bfloat16),
+    in_specs = [("qkv", step.qkv.view(np.int16), torch.bfloat16),
                 ("pos", step.positions, torch.int64),
                 ("slots", step.slot_mapping, torch.int32),
                 ("bt", step.block_tables, torch.int32),
@@ -343,31 +344,25 @@ def run_ours(args, rank, world, local_rank):
     dev_in = torch.empty(off, dtype=torch.uint8, device=dev_t)
     dv = {name: dev_in[offs[name]:offs[name] + arr.nbytes].view(dt).view(arr.shape)
           for name, arr, dt in in_specs}
-    dev_out = torch.empty(2, B, H, dtype=torch.bfloat16, device=dev_t)     # y, new residual
-    host_yr = torch.empty(2, B, H, dtype=torch.bfloat16).pin_memory()
+    host_x = torch.from_numpy(step.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host_r = torch.from_numpy(step.residual.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host_y = torch.empty(B, H, dtype=torch.bfloat16).pin_memory()
+    host_rout = torch.empty(B, H, dtype=torch.bfloat16).pin_memory()
     host_o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(arr.nbytes for _, arr, _ in in_specs)
-    d2h = host_yr.numel() * 2 + host_o.numel() * 2
-    side = torch.cuda.Stream(device=dev_t)
+    h2d = sum(arr.nbytes for _, arr, _ in in_specs) + 2 * host_x.numel() * 2
+    d2h = (host_y.numel() + host_rout.numel() + host_o.numel()) * 2
     q2, k2, v2 = decode_views(dv["qkv"])
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
-        e0, e1, ev_norm, ev_side = ev(), ev(), ev(), ev()
+        e0, e1 = ev(), ev()
         e0.record()
+        nv.nv_add_rmsnorm(host_x, host_r, d_g, host_y, host_rout, eps=wl.RMS_EPS)
         dev_in.copy_(host_in, non_blocking=True)
-        nv.nv_add_rmsnorm(dv["x"], dv["r"], d_g, dev_out[0], dev_out[1], eps=wl.RMS_EPS)
-        ev_norm.record()
-        side.wait_event(ev_norm)
-        with torch.cuda.stream(side):
-            host_yr.copy_(dev_out, non_blocking=True)
-            ev_side.record(side)
         nv.nv_qknorm_rope(q2, k2, d_qn, d_kn, table, dv["pos"], eps=wl.RMS_EPS, err_count=err)
         nv.nv_store_kvcache(k2, v2, kc, vc, dv["slots"], err)
-        nv.nv_decode_attn_paged(q2, kc, vc, dv["bt"], dv["ctx"], d_o, SCALE, workspace=ws,
+        nv.nv_decode_attn_paged(q2, kc, vc, dv["bt"], dv["ctx"], host_o, SCALE, workspace=ws,
                                 err_count=err)
-        host_o.copy_(d_o, non_blocking=True)
-        torch.cuda.current_stream().wait_event(ev_side)
         e1.record()
         torch.cuda.synchronize()
         if i >= args.warmup:

@@ -15,10 +15,19 @@
  * workspace query.
  *
  * Conventions shared by every entry point
- *   - Every tensor is a caller-owned DEVICE pointer (allocated e.g. by
- *     PyTorch).  The library never allocates, frees, synchronises or reads
- *     results back; every call only enqueues kernels on `stream` (a
- *     cudaStream_t; NULL means the legacy default stream) and returns.
+ *   - Every tensor is caller-owned memory the device can address: device
+ *     memory (allocated e.g. by PyTorch), or, for the tensors the kernels
+ *     touch only with ordinary loads and stores, pinned host memory mapped
+ *     into the device's address space (cudaHostAlloc / cudaHostRegister with
+ *     unified addressing, as on Grace-Blackwell), which the kernels then read
+ *     and write over the host link.  Tensors read through the tensor-memory
+ *     accelerator must be device (or managed) memory: the KV caches of
+ *     nv_decode_attn_paged and nv_prefill_attn_paged, and q, k, v of
+ *     nv_prefill_attn_varlen (q of nv_prefill_attn_paged too); these calls
+ *     return NV_EINVAL for anything else.  Everything else may be either.
+ *     The library never allocates, frees, synchronises or reads results
+ *     back; every call only enqueues kernels on `stream` (a cudaStream_t;
+ *     NULL means the legacy default stream) and returns.
  *   - bf16 tensors are passed as `nv_bf16_t` (the 16 raw bits of a bfloat16).
  *     Integer metadata is int32 (slot_mapping, block_tables, context_lens,
  *     cu_seqlens) except positions, which are int64, as in nano-vllm.

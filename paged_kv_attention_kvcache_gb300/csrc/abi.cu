@@ -14,6 +14,19 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensors read through TMA must be device (or managed) memory; pinned host
+// memory is fine only for the tensors the kernels touch with plain loads and
+// stores.  A host pointer here would make the tensor copy fault, so it is
+// rejected before anything is launched.
+bool tma_readable(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // do not leave the error for a later launch check
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
 int launch_status(cudaError_t e) { return e == cudaSuccess ? NV_OK : NV_ELAUNCH; }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -227,6 +240,7 @@ int nv_prefill_attn_varlen(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf
         !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)sched_counter & 3))
         return NV_EALIGN;
     if ((int64_t)(max_seqlen_q + 127) / 128 > 65535) return NV_EUNSUPPORTED;
+    if (!tma_readable(q) || !tma_readable(k) || !tma_readable(v)) return NV_EINVAL;
 
     CUtensorMap q_map, k_map, v_map;
     const uint32_t box[3] = {64, 1, 128};
@@ -283,6 +297,7 @@ int nv_prefill_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf1
         !aligned16(o) || ((uintptr_t)sched_counter & 3))
         return NV_EALIGN;
     if ((int64_t)(max_seqlen_q + 127) / 128 > 65535) return NV_EUNSUPPORTED;
+    if (!tma_readable(q) || !tma_readable(k_cache) || !tma_readable(v_cache)) return NV_EINVAL;
 
     CUtensorMap q_map, k_map, v_map;
     {
@@ -360,6 +375,7 @@ int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf16
     const size_t need = decode_workspace_bytes(B, Hq, max_splits);
     if (need > 0 && (!workspace || workspace_bytes < need)) return NV_EWORKSPACE;
     if (need > 0 && !aligned16(workspace)) return NV_EALIGN;
+    if (!tma_readable(k_cache) || !tma_readable(v_cache)) return NV_EINVAL;
 
     CUtensorMap k_map, v_map;
     const uint64_t dims[4] = {128, (uint64_t)Hkv, (uint64_t)block_size, (uint64_t)num_blocks};
