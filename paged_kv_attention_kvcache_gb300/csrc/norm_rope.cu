@@ -149,16 +149,14 @@ cudaError_t launch_add_rmsnorm(const uint16_t *x, const uint16_t *residual,
 constexpr int kRopeThreads = 256;
 
 // Normalise and rotate one 128-element head row.  The eight lanes of the
-// group named by `gmask` each hold elements [8j, 8j+8) and [64+8j, 64+8j+8)
-// of `src`; on return out1/out2 hold the lane's rotated elements as packed
-// bf16 pairs.  Shared by the in-place kernel and the fused cache-writing one
-// so that both give the same bits.
-__device__ __forceinline__ void norm_rope_row(const uint16_t *src, const uint16_t *__restrict__ w,
-                                              const float *__restrict__ cs_row, int j,
-                                              unsigned gmask, float eps, uint4 &out1,
-                                              uint4 &out2) {
-    uint4 a = *reinterpret_cast<const uint4 *>(src + 8 * j);
-    uint4 b = *reinterpret_cast<const uint4 *>(src + 64 + 8 * j);
+// group named by `gmask` each hold elements [8j, 8j+8) (in a) and
+// [64+8j, 64+8j+8) (in b) of the row; on return out1/out2 hold the lane's
+// rotated elements as packed bf16 pairs.  Shared by the in-place kernel and
+// the fused cache-writing one so that both give the same bits.
+__device__ __forceinline__ void norm_rope_regs(uint4 a, uint4 b, const uint16_t *__restrict__ w,
+                                               const float *__restrict__ cs_row, int j,
+                                               unsigned gmask, float eps, uint4 &out1,
+                                               uint4 &out2) {
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
     float x1[8], x2[8];
@@ -207,6 +205,33 @@ __device__ __forceinline__ void norm_rope_row(const uint16_t *src, const uint16_
     out2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
 }
 
+// The same, loading the lane's two vectors from `src` first.
+__device__ __forceinline__ void norm_rope_row(const uint16_t *src, const uint16_t *__restrict__ w,
+                                              const float *__restrict__ cs_row, int j,
+                                              unsigned gmask, float eps, uint4 &out1,
+                                              uint4 &out2) {
+    const uint4 a = *reinterpret_cast<const uint4 *>(src + 8 * j);
+    const uint4 b = *reinterpret_cast<const uint4 *>(src + 64 + 8 * j);
+    norm_rope_regs(a, b, w, cs_row, j, gmask, eps, out1, out2);
+}
+
+// Blocks of `kernel` (kRopeThreads each) resident at once on the current
+// device: the rotation kernels launch one such wave and loop over rows.
+template <typename Kernel>
+int64_t resident_grid(Kernel kernel) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRopeThreads, 0) !=
+            cudaSuccess)
+        return 152 * 4;
+    return (int64_t)(sms > 0 ? sms : 152) * (per_sm > 0 ? per_sm : 1);
+}
+
+// Each 8-lane group walks rows row0, row0 + groups, ... and loads the next
+// row's vectors and position before it normalises and rotates the current
+// one, so the SM always has loads in flight instead of running one dependent
+// load -> table -> compute chain per row and exiting.
 __global__ void __launch_bounds__(kRopeThreads)
 qknorm_rope_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restrict__ k,
                    int64_t k_stride, const uint16_t *__restrict__ qw,
@@ -218,31 +243,54 @@ qknorm_rope_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restr
     const int64_t n_rows = T * heads;
     const int lane = threadIdx.x & 31;
     const int j = lane & 7;                       // lane within the row group
-    const int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
+    const int64_t groups = (int64_t)gridDim.x * (kRopeThreads / 8);
+    int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
     if (row >= n_rows) return;
-    const int64_t t = row / heads;
-    const int h = (int)(row % heads);
-    uint16_t *base;
-    const uint16_t *w;
-    if (h < Hq) {
-        base = q + t * q_stride + (int64_t)h * 128;
-        w = qw;
-    } else {
-        base = k + t * k_stride + (int64_t)(h - Hq) * 128;
-        w = kw;
-    }
-    const int64_t pos = __ldg(positions + t);
-    if (pos < 0 || pos >= max_position) {
-        if (j == 0) count_error(err_count);
-        return;
-    }
-    // Groups of the same warp may have returned early, so the row's shuffles
-    // name only this group's lanes; all eight share the row and its position.
+    // Groups of the same warp may leave the loop at different rows, so the
+    // row's shuffles name only this group's lanes; all eight share the row.
     const unsigned gmask = 0xFFu << (lane & ~7);
-    uint4 o1, o2;
-    norm_rope_row(base, w, cos_sin + pos * 128, j, gmask, eps, o1, o2);
-    *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
-    *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
+    auto locate = [&](int64_t r, int64_t &t) {
+        t = r / heads;
+        const int h = (int)(r - t * heads);
+        return h < Hq ? q + t * q_stride + (int64_t)h * 128
+                      : k + t * k_stride + (int64_t)(h - Hq) * 128;
+    };
+    int64_t t;
+    uint16_t *base = locate(row, t);
+    const uint16_t *w = (row % heads) < Hq ? qw : kw;
+    uint4 a = *reinterpret_cast<const uint4 *>(base + 8 * j);
+    uint4 b = *reinterpret_cast<const uint4 *>(base + 64 + 8 * j);
+    int64_t pos = __ldg(positions + t);
+    for (;;) {
+        const int64_t next = row + groups;
+        const bool more = next < n_rows;
+        uint16_t *nbase = base;
+        int64_t nt = t;
+        uint4 na = a, nb = b;
+        int64_t npos = pos;
+        if (more) {
+            nbase = locate(next, nt);
+            na = *reinterpret_cast<const uint4 *>(nbase + 8 * j);
+            nb = *reinterpret_cast<const uint4 *>(nbase + 64 + 8 * j);
+            npos = __ldg(positions + nt);
+        }
+        if (pos < 0 || pos >= max_position) {
+            if (j == 0) count_error(err_count);
+        } else {
+            uint4 o1, o2;
+            norm_rope_regs(a, b, w, cos_sin + pos * 128, j, gmask, eps, o1, o2);
+            *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
+            *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
+        }
+        if (!more) break;
+        w = (next % heads) < Hq ? qw : kw;
+        row = next;
+        base = nbase;
+        t = nt;
+        a = na;
+        b = nb;
+        pos = npos;
+    }
 }
 
 cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64_t k_stride,
@@ -252,7 +300,9 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
     const int64_t rows = T * (Hq + Hkv);
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
-    const unsigned blocks = (unsigned)((threads + kRopeThreads - 1) / kRopeThreads);
+    static const int64_t resident = resident_grid(qknorm_rope_kernel);
+    int64_t blocks = (threads + kRopeThreads - 1) / kRopeThreads;
+    if (blocks > resident) blocks = resident;
     return launch_pdl(qknorm_rope_kernel, dim3(blocks), dim3(kRopeThreads), (size_t)0, s, q,
                       q_stride, k, k_stride, qw, kw, cos_sin, max_position, positions, T, Hq, Hkv,
                       eps, err_count);
@@ -267,7 +317,9 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
 // asked), v rows are copied bit for bit to the slot.  Eight lanes per row as
 // above; k never makes the extra round trip through HBM that the separate
 // store kernel would read it back for.
-__global__ void __launch_bounds__(kRopeThreads)
+// Four blocks per SM (64 registers, a few bytes spilled) measured faster
+// than three without the spill: the loads in flight per SM are what count.
+__global__ void __launch_bounds__(kRopeThreads, 4)
 qknorm_rope_store_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restrict__ k,
                          int64_t k_stride, const uint16_t *__restrict__ v, int64_t v_stride,
                          const uint16_t *__restrict__ qw, const uint16_t *__restrict__ kw,
@@ -281,49 +333,76 @@ qknorm_rope_store_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *_
     const int64_t n_rows = T * heads;
     const int lane = threadIdx.x & 31;
     const int j = lane & 7;
-    const int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
-    if (row >= n_rows) return;
-    const int64_t t = row / heads;
-    const int h = (int)(row % heads);
+    const int64_t groups = (int64_t)gridDim.x * (kRopeThreads / 8);
     const int64_t D = (int64_t)Hkv * 128;
-    int64_t slot = -1;
-    if (h >= Hq) {
-        slot = __ldg(slot_mapping + t);
+    int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
+    if (row >= n_rows) return;
+    const unsigned gmask = 0xFFu << (lane & ~7);
+    // Grid-stride over rows as in qknorm_rope_kernel: the next row's vectors,
+    // position and slot are in flight while the current row is processed.
+    auto source = [&](int64_t t, int h) -> uint16_t * {
+        if (h < Hq) return q + t * q_stride + (int64_t)h * 128;
+        if (h < Hq + Hkv) return k + t * k_stride + (int64_t)(h - Hq) * 128;
+        return const_cast<uint16_t *>(v) + t * v_stride + (int64_t)(h - Hq - Hkv) * 128;
+    };
+    int64_t t = row / heads;
+    int h = (int)(row - t * heads);
+    uint16_t *base = source(t, h);
+    uint4 a = *reinterpret_cast<const uint4 *>(base + 8 * j);
+    uint4 b = *reinterpret_cast<const uint4 *>(base + 64 + 8 * j);
+    int64_t pos = __ldg(positions + t);
+    int64_t slot = h >= Hq ? (int64_t)__ldg(slot_mapping + t) : -1;
+    for (;;) {
+        const int64_t next = row + groups;
+        const bool more = next < n_rows;
+        int64_t nt = t, npos = pos, nslot = slot;
+        int nh = h;
+        uint16_t *nbase = base;
+        uint4 na = a, nb = b;
+        if (more) {
+            nt = next / heads;
+            nh = (int)(next - nt * heads);
+            nbase = source(nt, nh);
+            na = *reinterpret_cast<const uint4 *>(nbase + 8 * j);
+            nb = *reinterpret_cast<const uint4 *>(nbase + 64 + 8 * j);
+            npos = __ldg(positions + nt);
+            nslot = nh >= Hq ? (int64_t)__ldg(slot_mapping + nt) : -1;
+        }
         if (slot != -1 && (slot < 0 || slot >= num_slots)) {
             if (j == 0 && h == Hq) count_error(err_count);   // once per token
             slot = -1;
         }
-    }
-    if (h >= Hq + Hkv) {                                        // v: a bit copy
-        if (slot < 0) return;
-        const int hv = h - Hq - Hkv;
-        const uint16_t *src = v + t * v_stride + (int64_t)hv * 128;
-        uint16_t *dst = v_cache + slot * D + (int64_t)hv * 128;
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src + 8 * j));
-        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 64 + 8 * j));
-        *reinterpret_cast<uint4 *>(dst + 8 * j) = a;
-        *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = b;
-        return;
-    }
-    const bool is_q = h < Hq;
-    uint16_t *base = is_q ? q + t * q_stride + (int64_t)h * 128
-                          : k + t * k_stride + (int64_t)(h - Hq) * 128;
-    const int64_t pos = __ldg(positions + t);
-    if (pos < 0 || pos >= max_position) {
-        if (j == 0) count_error(err_count);
-        return;
-    }
-    const unsigned gmask = 0xFFu << (lane & ~7);
-    uint4 o1, o2;
-    norm_rope_row(base, is_q ? qw : kw, cos_sin + pos * 128, j, gmask, eps, o1, o2);
-    if (is_q || write_k) {
-        *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
-        *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
-    }
-    if (!is_q && slot >= 0) {
-        uint16_t *dst = k_cache + slot * D + (int64_t)(h - Hq) * 128;
-        *reinterpret_cast<uint4 *>(dst + 8 * j) = o1;
-        *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = o2;
+        if (h >= Hq + Hkv) {                                    // v: a bit copy
+            if (slot >= 0) {
+                uint16_t *dst = v_cache + slot * D + (int64_t)(h - Hq - Hkv) * 128;
+                *reinterpret_cast<uint4 *>(dst + 8 * j) = a;
+                *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = b;
+            }
+        } else if (pos < 0 || pos >= max_position) {
+            if (j == 0) count_error(err_count);
+        } else {
+            const bool is_q = h < Hq;
+            uint4 o1, o2;
+            norm_rope_regs(a, b, is_q ? qw : kw, cos_sin + pos * 128, j, gmask, eps, o1, o2);
+            if (is_q || write_k) {
+                *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
+                *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
+            }
+            if (!is_q && slot >= 0) {
+                uint16_t *dst = k_cache + slot * D + (int64_t)(h - Hq) * 128;
+                *reinterpret_cast<uint4 *>(dst + 8 * j) = o1;
+                *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = o2;
+            }
+        }
+        if (!more) break;
+        row = next;
+        t = nt;
+        h = nh;
+        base = nbase;
+        a = na;
+        b = nb;
+        pos = npos;
+        slot = nslot;
     }
 }
 
@@ -338,7 +417,9 @@ cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
     const int64_t rows = T * (Hq + 2 * Hkv);
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
-    const unsigned blocks = (unsigned)((threads + kRopeThreads - 1) / kRopeThreads);
+    static const int64_t resident = resident_grid(qknorm_rope_store_kernel);
+    int64_t blocks = (threads + kRopeThreads - 1) / kRopeThreads;
+    if (blocks > resident) blocks = resident;
     return launch_pdl(qknorm_rope_store_kernel, dim3(blocks), dim3(kRopeThreads), (size_t)0, s, q,
                       q_stride, k, k_stride, v, v_stride, qw, kw, cos_sin, max_position,
                       positions, slot_mapping, k_cache, v_cache, num_slots, T, Hq, Hkv, eps,

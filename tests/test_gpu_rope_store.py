@@ -149,3 +149,40 @@ def test_fused_rope_store_counts_bad_slots_and_positions():
     ref_vc.reshape(-1, D)[slots[9]] = qkv[9, Q + D:]
     check_cache_rows(got_kc, ref_kc, "k cache with bad tokens")
     assert np.array_equal(got_vc, ref_vc)
+
+
+def test_bad_tokens_in_late_passes_of_the_grid():
+    # A batch of several times the resident grid's rows, so each row group
+    # walks many rows; the bad slots and positions sit in late passes and at
+    # the very last tokens.  Both the fused pass and the in-place rotation
+    # must skip and count exactly those rows and give the same bits elsewhere.
+    s = wl.QWEN3_8B
+    qkv, pos, slots, qn, kn, kc0, vc0 = _inputs(630, s, [1000, 1500, 700])
+    T, Q, D = qkv.shape[0], s.q_size, s.kv_size
+    num_slots = kc0.shape[0] * kc0.shape[1]
+    slots, pos = slots.copy(), pos.copy()
+    slots[2900], slots[T - 1] = num_slots + 5, -3
+    pos[3100], pos[T - 2] = -1, wl.MAX_POSITION
+    got_qkv, got_kc, got_vc, err = _run_fused(qkv, pos, slots, qn, kn, kc0, vc0, s, True)
+    assert err == 2 + 2 * (s.hq + s.hkv)
+    for t in (3100, T - 2):
+        assert np.array_equal(got_qkv[t], qkv[t]), "token with a bad position stays untouched"
+    good = np.ones(T, bool)
+    good[[2900, 3100, T - 2, T - 1]] = False
+    q_rot, k_rot, ref_kc, ref_vc = _oracle(qkv[good], pos[good], slots[good], qn, kn, kc0, vc0, s)
+    check_close(got_qkv[good, :Q], q_rot.reshape(-1, Q), "q of good tokens")
+    check_close(got_qkv[good, Q:Q + D], k_rot.reshape(-1, D), "k of good tokens")
+    for t in (3100, T - 2):                      # v rows of bad-position tokens are still copied
+        ref_vc.reshape(-1, D)[slots[t]] = qkv[t, Q + D:]
+    check_cache_rows(got_kc, ref_kc, "k cache with late bad tokens")
+    assert np.array_equal(got_vc, ref_vc)
+
+    table = rope_table()
+    d_qkv = dev(qkv)
+    q, k, _ = _views(d_qkv, s)
+    err_t = err_counter()
+    nv.nv_qknorm_rope(q, k, dev(qn), dev(kn), table, dev_i64(pos), eps=wl.RMS_EPS,
+                      err_count=err_t)
+    torch.cuda.synchronize()
+    assert int(err_t.item()) == 2 * (s.hq + s.hkv)
+    assert np.array_equal(host(d_qkv), got_qkv), "in-place rotation gives the fused pass's bits"
