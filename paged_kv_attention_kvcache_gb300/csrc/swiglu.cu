@@ -4,21 +4,38 @@
 // out[t][i] = silu(gate_i) * up_i, computed in fp32 and rounded once to bf16.
 // Pure streaming: every input byte is read once and every output byte written
 // once, so the kernel is HBM-bound.  A thread moves 16-byte vectors (eight
-// elements of gate and the matching eight of up) and keeps kUnroll of them in
-// flight; the grid is a whole number of waves over the 152 SMs.
+// elements of gate and the matching eight of up), walking them with the
+// grid's stride, and loads its next kSwigluPipe vectors before it computes
+// and stores the current ones, so loads stay in flight while it computes; the
+// grid is one resident wave over the 152 SMs.
 #include "common.cuh"
 #include "internal.h"
 
 namespace nvattn {
 
 constexpr int kSwigluThreads = 256;
-constexpr int kSwigluUnroll = 4;
+constexpr int kSwigluPipe = 2;
 constexpr int kSwigluBlocksPerSm = 4;   // 64 registers x 256 threads: four resident
 constexpr int kNumSms = 152;
 
 __device__ __forceinline__ float silu_times(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
+
+// (token, vector) of a flat vector index, advanced by a fixed stride without
+// a 64-bit division per step.
+struct VecCursor {
+    int64_t t;
+    int c;
+    __device__ __forceinline__ void advance(int64_t dt, int dc, int nvec) {
+        t += dt;
+        c += dc;
+        if (c >= nvec) {
+            c -= nvec;
+            ++t;
+        }
+    }
+};
 
 // `out` may be `x` itself (same token stride): element (t, i) of the output
 // then overwrites gate (t, i), which only the same thread has read.
@@ -28,24 +45,38 @@ silu_and_mul_kernel(const uint4 *x, int64_t x_stride_v, uint4 *out, int64_t out_
     pdl_wait_release();
     const int64_t total = T * nvec;
     const int64_t stride = (int64_t)gridDim.x * kSwigluThreads;
-    for (int64_t base = (int64_t)blockIdx.x * kSwigluThreads + threadIdx.x; base < total;
-         base += stride * kSwigluUnroll) {
-        uint4 g[kSwigluUnroll], u[kSwigluUnroll];
-        int64_t t[kSwigluUnroll], c[kSwigluUnroll];
+    const int64_t dt = stride / nvec;
+    const int dc = (int)(stride - dt * nvec);
+    int64_t idx = (int64_t)blockIdx.x * kSwigluThreads + threadIdx.x;
+    if (idx >= total) return;
+    VecCursor cur{idx / nvec, (int)(idx % nvec)};
+    VecCursor ahead = cur;
+    uint4 g[kSwigluPipe], u[kSwigluPipe];
+    // The next kSwigluPipe vectors of this thread are loaded before the current
+    // ones are computed and stored.
 #pragma unroll
-        for (int k = 0; k < kSwigluUnroll; ++k) {
-            const int64_t idx = base + k * stride;
-            t[k] = idx / nvec;
-            c[k] = idx - t[k] * nvec;
-            if (idx < total) {
-                const uint4 *row = x + t[k] * x_stride_v;
-                g[k] = row[c[k]];
-                u[k] = row[nvec + c[k]];
+    for (int k = 0; k < kSwigluPipe; ++k) {
+        if (idx + k * stride < total) {
+            const uint4 *row = x + ahead.t * x_stride_v;
+            g[k] = row[ahead.c];
+            u[k] = row[nvec + ahead.c];
+        }
+        ahead.advance(dt, dc, nvec);
+    }
+    for (; idx < total; idx += kSwigluPipe * stride) {
+        uint4 ng[kSwigluPipe], nu[kSwigluPipe];
+#pragma unroll
+        for (int k = 0; k < kSwigluPipe; ++k) {
+            if (idx + (kSwigluPipe + k) * stride < total) {
+                const uint4 *row = x + ahead.t * x_stride_v;
+                ng[k] = row[ahead.c];
+                nu[k] = row[nvec + ahead.c];
             }
+            ahead.advance(dt, dc, nvec);
         }
 #pragma unroll
-        for (int k = 0; k < kSwigluUnroll; ++k) {
-            if (base + k * stride < total) {
+        for (int k = 0; k < kSwigluPipe; ++k) {
+            if (idx + k * stride < total) {
                 const uint32_t gw[4] = {g[k].x, g[k].y, g[k].z, g[k].w};
                 const uint32_t uw[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
                 uint32_t o[4];
@@ -53,8 +84,11 @@ silu_and_mul_kernel(const uint4 *x, int64_t x_stride_v, uint4 *out, int64_t out_
                 for (int e = 0; e < 4; ++e)
                     o[e] = pack_bf16x2(silu_times(bf16_lo(gw[e]), bf16_lo(uw[e])),
                                        silu_times(bf16_hi(gw[e]), bf16_hi(uw[e])));
-                out[t[k] * out_stride_v + c[k]] = make_uint4(o[0], o[1], o[2], o[3]);
+                out[cur.t * out_stride_v + cur.c] = make_uint4(o[0], o[1], o[2], o[3]);
             }
+            cur.advance(dt, dc, nvec);
+            g[k] = ng[k];
+            u[k] = nu[k];
         }
     }
 }
@@ -64,7 +98,7 @@ cudaError_t launch_silu_and_mul(const uint16_t *x, int64_t x_stride, uint16_t *o
     const int nvec = I / 8;
     const int64_t total = T * nvec;
     if (total == 0) return cudaSuccess;
-    const int64_t per_block = (int64_t)kSwigluThreads * kSwigluUnroll;
+    const int64_t per_block = (int64_t)kSwigluThreads * kSwigluPipe;
     int64_t blocks = (total + per_block - 1) / per_block;
     const int64_t wave = (int64_t)kNumSms * kSwigluBlocksPerSm;
     if (blocks > wave) blocks = wave;
