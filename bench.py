@@ -372,6 +372,7 @@ def run_ours(args, rank, world, local_rank):
 
     graph_info = graph_decode_overhead(dev_t)
     decode_sets = decode_attention_configs(dev_t)
+    prefix_prefill = prefill_prefix_config(dev_t)
 
     # ---- QK-Norm + RoPE + store on the prefill batch: two kernels vs one pass
     def time_us(fn, reps=20):
@@ -416,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
 
     return dict(
         graph=graph_info, rope_store=rope_store, swiglu=swiglu, decode_sets=decode_sets,
+        prefix_prefill=prefix_prefill,
         value=value, ms_per_step=tot_ms / args.steps, dec_ms=statistics.mean(dec_ms),
         pre_ms=statistics.mean(pre_ms), attn_ms=statistics.mean(attn_ms),
         attn_gbs=attn_gbs, ptflops=ptflops, pattn_ms=pattn_sum / args.steps, clocks=clk,
@@ -471,6 +473,64 @@ def decode_attention_configs(dev_t, reps: int = 20):
                                                       "gbs": nbytes / t / 1e9}
         del kc, vc
     del flush
+    return out
+
+
+# ------------------------------------ prefill over the paged cache (prefix hit)
+def prefill_prefix_config(dev_t, reps: int = 20):
+    """Prefill over the paged cache on the prefix-hit workload (Qwen3-8B heads,
+    16 sequences, cached prefixes of 256..4096 tokens, 128..1024 new ones):
+    nv_prefill_attn_paged, and nv_prefill_attn_varlen over the same keys
+    gathered into contiguous rows.  FLOPs count the causal pairs only,
+    4*d*Hq*sum(L*P + L*(L+1)/2).  L2 flushed before each rep; median of `reps`
+    event-timed launches."""
+    import torch
+    import paged_kv_attention_kvcache_gb300 as nv
+    pre = wl.config_prefix()
+    s = pre.shape
+    L = pre.new.astype(np.float64)
+    P = pre.prefix.astype(np.float64)
+    flops = float((4 * 128 * s.hq * (L * P + L * (L + 1) / 2)).sum())
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).to(dev_t)
+
+    def dev_i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev_t)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev_t)
+    q, kc, vc = dev(pre.q), dev(pre.pool.k), dev(pre.pool.v)
+    kk, vv = wl.gather_paged(pre.pool, pre.block_tables, pre.prefix + pre.new)
+    dk, dvv = dev(kk), dev(vv)
+    bt, cu_q, cu_k = dev_i32(pre.block_tables), dev_i32(pre.cu_seqlens_q), dev_i32(
+        pre.cu_seqlens_k)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev_t)
+    sched = torch.zeros(1, dtype=torch.int32, device=dev_t)
+    mq, mk = int(pre.new.max()), int((pre.prefix + pre.new).max())
+    calls = {
+        "paged": lambda: nv.nv_prefill_attn_paged(q, kc, vc, bt, o, cu_q, cu_k, mq, SCALE,
+                                                  sched_counter=sched),
+        "contiguous": lambda: nv.nv_prefill_attn_varlen(q, dk, dvv, o, cu_q, cu_k, mq, mk,
+                                                        SCALE, sched_counter=sched),
+    }
+    out = {"workload": "qwen3_8b_16seq_prefix256x1-16_new128-1024", "tokens_new": int(L.sum()),
+           "tokens_cached": int(P.sum()), "flops": flops}
+    for name, fn in calls.items():
+        times = []
+        for i in range(reps + 3):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) / 1e3)
+        t = statistics.median(times)
+        out[name] = {"ms": t * 1e3, "tflops": flops / t / 1e12}
+    del flush, kc, vc, dk, dvv
     return out
 
 
@@ -796,6 +856,7 @@ def main():
             "nominal_frac": {"decode_attn_of_7900_GBs": r["attn_gbs"] / 7900.0,
                              "prefill_of_2250_TFLOPs": r["ptflops"] / 2250.0},
             "decode_attention_sets": r["decode_sets"],
+            "prefill_paged_prefix": r["prefix_prefill"],
             "decode_graph": r["graph"],
             "rope_store_prefill": r["rope_store"],
             "silu_and_mul_prefill": r["swiglu"],

@@ -227,3 +227,38 @@ def test_prefill_paged_other_block_sizes(bs):
     got, ref = _paged_case(580 + bs, prefix=[0, 37, 256, 300, 640], new=[5, 130, 128, 200, 300],
                            hq=8, hkv=2, bs=bs)
     check_close(got, ref, f"paged prefill bs={bs}")
+
+
+def test_prefill_paged_prefix_workload_full_size_sampled():
+    # The measured prefix-hit workload at full size, in the launch the bench
+    # times (dynamic queue): 16 sequences, block-aligned cached prefixes of
+    # 256..4096 tokens and 128..1024 new ones; first/last query of every
+    # sequence plus random rows, every head drawn.  The contiguous kernel over
+    # the same keys gathered from the pool must agree with it bit for bit.
+    pre = wl.config_prefix()
+    s = pre.shape
+    Tq = int(pre.new.sum())
+    cu_q, cu_k = pre.cu_seqlens_q, pre.cu_seqlens_k
+    o = torch.empty(Tq, s.hq, 128, dtype=torch.bfloat16, device="cuda")
+    err = err_counter()
+    nv.nv_prefill_attn_paged(dev(pre.q), dev(pre.pool.k), dev(pre.pool.v),
+                             dev_i32(pre.block_tables), o, dev_i32(cu_q), dev_i32(cu_k),
+                             int(pre.new.max()), SCALE, err_count=err,
+                             sched_counter=sched_counter(True))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    g = np.random.default_rng(590)
+    toks = np.concatenate([cu_q[:-1], cu_q[1:] - 1, g.integers(0, Tq, 400)])
+    rows = np.stack([toks, g.integers(0, s.hq, toks.size)], axis=1).astype(np.int64)
+    ref = oracle.attention_paged_prefill(pre.q, pre.pool.k, pre.pool.v, pre.block_tables,
+                                         cu_q, cu_k, SCALE, rows=rows)
+    got = host(o)
+    check_close(got[rows[:, 0], rows[:, 1]], ref, "prefix-hit workload, sampled rows")
+
+    kk, vv = wl.gather_paged(pre.pool, pre.block_tables, pre.prefix + pre.new)
+    o2 = torch.empty_like(o)
+    nv.nv_prefill_attn_varlen(dev(pre.q), dev(kk), dev(vv), o2, dev_i32(cu_q), dev_i32(cu_k),
+                              int(pre.new.max()), int((pre.prefix + pre.new).max()), SCALE,
+                              sched_counter=sched_counter(True))
+    torch.cuda.synchronize()
+    assert np.array_equal(host(o2), got), "paged and contiguous keys give the same bits"

@@ -321,3 +321,50 @@ def config5(seed: int = 1005, batch: int = 32, num_blocks: int = 6000):
     ctx = np.clip(np.floor(np.exp(u)), 4096, 40960).astype(np.int32)
     return make_decode(seed, QWEN3_8B, ctx, num_blocks, with_norms=False,
                        k_outlier_frac=0.01, name="cfg5")
+
+
+# ------------------------------------------ prefill over the paged cache
+@dataclass
+class PrefixPrefill:
+    """Prefill of `new` tokens per sequence whose first `prefix` tokens are
+    already in the paged cache (a prefix-cache hit, or the earlier chunks of a
+    chunked prefill).  The pool holds all prefix + new K/V rows of every
+    sequence; q holds the new tokens' queries, packed."""
+    shape: Shape
+    prefix: np.ndarray           # [B] int64, multiples of the block size
+    new: np.ndarray              # [B] int64
+    cu_seqlens_q: np.ndarray     # [B+1] int32
+    cu_seqlens_k: np.ndarray     # [B+1] int32
+    block_tables: np.ndarray     # [B, MB] int32
+    pool: PagedPool
+    q: np.ndarray                # [sum(new), Hq, d] bf16 bits
+    name: str = ""
+
+
+def config_prefix(seed: int = 1006, n_seqs: int = 16):
+    """Qwen3-8B heads, 16 sequences with a cached prefix of 256 * U{1..16}
+    tokens (prefix caching works in whole blocks) and U[128, 1024] new tokens."""
+    g = rng(seed, "pfx.lens")
+    prefix = BLOCK_SIZE * g.integers(1, 16, size=n_seqs, endpoint=True).astype(np.int64)
+    new = g.integers(128, 1024, size=n_seqs, endpoint=True).astype(np.int64)
+    lk = prefix + new
+    nb = int(sum(math.ceil(int(L) / BLOCK_SIZE) for L in lk))
+    perm = rng(seed, "pfx.perm").permutation(nb).astype(np.int32)
+    bt = carve_block_tables(perm, lk)
+    pool = make_pool(seed, nb, bt[bt >= 0], QWEN3_8B.hkv)
+    q = normal_bf16(seed, "pfx.q", (int(new.sum()), QWEN3_8B.hq, HEAD_DIM))
+    return PrefixPrefill(shape=QWEN3_8B, prefix=prefix, new=new, cu_seqlens_q=cu_seqlens(new),
+                         cu_seqlens_k=cu_seqlens(lk), block_tables=bt, pool=pool, q=q,
+                         name="prefix")
+
+
+def gather_paged(pool: PagedPool, block_tables: np.ndarray, lengths) -> tuple:
+    """The K and V rows of each sequence, in order, packed [sum(lengths), Hkv, d]
+    (the contiguous layout of the same keys)."""
+    ks, vs = [], []
+    for b, L in enumerate(np.asarray(lengths)):
+        L = int(L)
+        ids = block_tables[b, :math.ceil(L / BLOCK_SIZE)]
+        ks.append(pool.k[ids].reshape(-1, pool.hkv, pool.k.shape[-1])[:L])
+        vs.append(pool.v[ids].reshape(-1, pool.hkv, pool.v.shape[-1])[:L])
+    return np.concatenate(ks), np.concatenate(vs)
