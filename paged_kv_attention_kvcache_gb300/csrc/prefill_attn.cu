@@ -28,10 +28,12 @@
 //    softmax warpgroup work while the tensor core serves the other.
 //  - Warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1:
 //    one row per thread (TMEM lane = row).  tcgen05.ld of the S row, causal
-//    mask on the diagonal tile, online softmax in base 2 with a lazy rescale
-//    (O_a in TMEM is rescaled only when the row max grows by more than 2^8,
-//    so the stale max bounds p by 256), and P written back as packed bf16
-//    over the first 64 columns of S_a, where the PV MMA reads it.  The commit
+//    mask on the diagonal tile (an unmasked tile's row max comes from the
+//    loads themselves, tcgen05.ld.red.max), online softmax in base 2 with a
+//    lazy rescale (O_a in TMEM is rescaled only when the row max grows by
+//    more than 2^8, so the stale max bounds p by 256), and P written back as
+//    packed bf16 over the first 64 columns of S_a, where the PV MMA reads
+//    it.  The commit
 //    that signals S_a,j also covers PV_a,j-1 (issued before it), so a rescale
 //    of O_a after S_a,j has landed never races the tensor core.
 //  - Epilogue: O_a / l straight to global memory with predicated 16-byte
@@ -200,6 +202,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+// The maximum of the thread's 32 fp32 columns, reduced by the load itself
+// (tcgen05.ld.red, sm_103a).  The loaded values are not used.
+__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr) {
+    uint32_t r[32];
+    float mx;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=f"(mx)
+        : "r"(taddr));
+    return mx;
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -611,20 +632,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                 for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
                 if (!diag) {
-                    // The next chunk's load is in flight while this one is reduced.
-                    uint32_t rb[2][32];
-                    tmem_ld32(lane_addr + col_s, rb[0]);
+                    // The loads reduce: four chunk maxima, one wait.
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mx4[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
-                        const uint32_t (&r)[32] = rb[c & 1];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            mx4[e & 3] = fmax3(mx4[e & 3], __uint_as_float(r[2 * e]),
-                                               __uint_as_float(r[2 * e + 1]));
-                        if (c < 3) tmem_wait_ld();
-                    }
+                    // Tie the maxima to the wait so no use is scheduled above it.
+                    asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
                 } else {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
