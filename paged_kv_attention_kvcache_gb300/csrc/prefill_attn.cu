@@ -639,14 +639,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     // Tie the maxima to the wait so no use is scheduled above it.
                     asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
                 } else {
+                    // Masked: the next chunk's load is in flight while this one is reduced.
+                    uint32_t rb[2][32];
+                    tmem_ld32(lane_addr + col_s, rb[0]);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_addr + col_s + c * 32, r);
-                        tmem_wait_ld();
+                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                        const uint32_t (&r)[32] = rb[c & 1];
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e <= vis) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(r[e]));
+                        if (c < 3) tmem_wait_ld();
                     }
                 }
                 const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
@@ -700,11 +704,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         tmem_st16(lane_addr + col_s + c * 16, pk);
                     }
                 } else {
+                    uint32_t rb[2][32];
+                    tmem_ld32(lane_addr + col_s, rb[0]);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_addr + col_s + c * 32, r);
-                        tmem_wait_ld();
+                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                        const uint32_t (&r)[32] = rb[c & 1];
                         uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
@@ -714,6 +720,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                             sum4[e & 3] += p0 + p1;
                             pk[e] = pack_bf16x2(p0, p1);
                         }
+                        if (c < 3) tmem_wait_ld();
                         tmem_st16(lane_addr + col_s + c * 16, pk);
                     }
                 }
@@ -734,11 +741,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const int qpos = it.q0 + a * kBM + row;
             const float inv_l = 1.f / l;
             uint16_t *orow = p.o + ((int64_t)(it.q_start + qpos) * p.Hq + it.h) * 128;
+            uint32_t rb[2][32];
+            tmem_ld32(lane_addr + col_o, rb[0]);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + col_o + c * 32, r);
-                tmem_wait_ld();
+                if (c < 3) tmem_ld32(lane_addr + col_o + (c + 1) * 32, rb[(c + 1) & 1]);
+                const uint32_t (&r)[32] = rb[c & 1];
                 if (qpos < it.L) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -750,11 +759,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) = v;
                     }
                 }
+                if (c < 3) tmem_wait_ld();
+                if (c == 2) {
+                    // All of O_a is in registers: the next item's first PV may
+                    // overwrite it while the last chunk is stored.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->o_empty[a]);
+                }
             }
-            // O_a may now be overwritten by the next item's first PV.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->o_empty[a]);
             release_item(bars, n, lane);
         }
         if (!ok) record_failure(bars, p.err_count);
