@@ -11,6 +11,20 @@
 
 namespace nvattn {
 
+// Blocks of `kernel` (with `threads` threads and no dynamic shared memory)
+// resident at once on the current device: grid-stride kernels launch one
+// such wave.  Falls back to 152 SMs x `fallback_per_sm` if a query fails.
+template <typename... KArgs>
+inline int64_t resident_grid(void (*kernel)(KArgs...), int threads, int fallback_per_sm) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) !=
+            cudaSuccess || sms <= 0 || per_sm <= 0)
+        return (int64_t)152 * fallback_per_sm;
+    return (int64_t)sms * per_sm;
+}
+
 // Launch with programmatic stream serialization (see pdl_wait_release).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

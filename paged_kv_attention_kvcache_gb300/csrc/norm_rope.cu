@@ -215,19 +215,6 @@ __device__ __forceinline__ void norm_rope_row(const uint16_t *src, const uint16_
     norm_rope_regs(a, b, w, cs_row, j, gmask, eps, out1, out2);
 }
 
-// Blocks of `kernel` (kRopeThreads each) resident at once on the current
-// device: the rotation kernels launch one such wave and loop over rows.
-template <typename Kernel>
-int64_t resident_grid(Kernel kernel) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRopeThreads, 0) !=
-            cudaSuccess)
-        return 152 * 4;
-    return (int64_t)(sms > 0 ? sms : 152) * (per_sm > 0 ? per_sm : 1);
-}
-
 // Each 8-lane group walks rows row0, row0 + groups, ... and loads the next
 // row's vectors and position before it normalises and rotates the current
 // one, so the SM always has loads in flight instead of running one dependent
@@ -300,7 +287,7 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
     const int64_t rows = T * (Hq + Hkv);
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
-    static const int64_t resident = resident_grid(qknorm_rope_kernel);
+    static const int64_t resident = resident_grid(qknorm_rope_kernel, kRopeThreads, 4);
     int64_t blocks = (threads + kRopeThreads - 1) / kRopeThreads;
     if (blocks > resident) blocks = resident;
     return launch_pdl(qknorm_rope_kernel, dim3(blocks), dim3(kRopeThreads), (size_t)0, s, q,
@@ -417,7 +404,7 @@ cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
     const int64_t rows = T * (Hq + 2 * Hkv);
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
-    static const int64_t resident = resident_grid(qknorm_rope_store_kernel);
+    static const int64_t resident = resident_grid(qknorm_rope_store_kernel, kRopeThreads, 4);
     int64_t blocks = (threads + kRopeThreads - 1) / kRopeThreads;
     if (blocks > resident) blocks = resident;
     return launch_pdl(qknorm_rope_store_kernel, dim3(blocks), dim3(kRopeThreads), (size_t)0, s, q,

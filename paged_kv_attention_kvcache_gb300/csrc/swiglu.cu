@@ -7,7 +7,7 @@
 // elements of gate and the matching eight of up), walking them with the
 // grid's stride, and loads its next kSwigluPipe vectors before it computes
 // and stores the current ones, so loads stay in flight while it computes; the
-// grid is one resident wave over the 152 SMs.
+// grid is one resident wave (four 256-thread blocks per SM at 64 registers).
 #include "common.cuh"
 #include "internal.h"
 
@@ -15,8 +15,6 @@ namespace nvattn {
 
 constexpr int kSwigluThreads = 256;
 constexpr int kSwigluPipe = 2;
-constexpr int kSwigluBlocksPerSm = 4;   // 64 registers x 256 threads: four resident
-constexpr int kNumSms = 152;
 
 __device__ __forceinline__ float silu_times(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
@@ -100,7 +98,7 @@ cudaError_t launch_silu_and_mul(const uint16_t *x, int64_t x_stride, uint16_t *o
     if (total == 0) return cudaSuccess;
     const int64_t per_block = (int64_t)kSwigluThreads * kSwigluPipe;
     int64_t blocks = (total + per_block - 1) / per_block;
-    const int64_t wave = (int64_t)kNumSms * kSwigluBlocksPerSm;
+    static const int64_t wave = resident_grid(silu_and_mul_kernel, kSwigluThreads, 4);
     if (blocks > wave) blocks = wave;
     return launch_pdl(silu_and_mul_kernel, dim3((unsigned)blocks), dim3(kSwigluThreads), (size_t)0,
                       s, (const uint4 *)x, x_stride / 8, (uint4 *)out, out_stride / 8, T, nvec);
