@@ -139,6 +139,17 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// Plain bulk copy global -> shared through the async proxy (both addresses
+// 16-byte aligned, bytes a multiple of 16), completing on `bar`'s tx count.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------- warp-level tensor
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                             uint32_t &r2, uint32_t &r3) {

@@ -87,10 +87,15 @@ struct Barriers {
     uint64_t k_empty[kKStages], v_empty[kVStages];
     uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles], o_empty[kQTiles];
     uint64_t item_full[kItemRing], item_empty[kItemRing];
+    uint64_t v_clean;           // paged: the last V tile's rows past Lk are zeroed
     Item item[kItemRing];       // decoded items; n_kv < 0 = no more work
     uint32_t tmem_base;
     int failed;
 };
+
+// Zeros copied over the rows past Lk of a paged item's last V tile (one
+// 64-dim half: at most 127 rows of 128 bytes).
+__device__ __align__(128) uint8_t g_zero_rows[kHalf];
 
 // Returns false for an item with no rows; *bad is set when the sequence is
 // malformed (Lk < Lq), in which case no role touches it.
@@ -336,6 +341,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&bars->item_full[r], 1);
             mbar_init(&bars->item_empty[r], kItemReaders);
         }
+        mbar_init(&bars->v_clean, 1);
         bars->failed = 0;
         fence_mbarrier_init();
     }
@@ -455,8 +461,29 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (ok) ok = load_v(it, j);
                 }
                 if (!ok) break;
+                // Paged: rows past Lk of the item's last V tile (slot `zc`) are
+                // zeroed once the next item has been drawn (the atomic's latency
+                // overlaps the tile's landing).
+                const int ztail = kPaged ? it.Lk - (it.n_kv - 1) * kBN : kBN;
+                const int zc = vcnt - 1;
                 fetch(it);
                 ok = publish(it);
+                if (ok && kPaged && ztail < kBN) {
+                    // Cache rows past Lk may hold any bits; their probability is
+                    // zero but 0 * NaN is not.  Once the tile has landed, its rows
+                    // past Lk are overwritten by two bulk copies of zeros from
+                    // global memory (async proxy, like the tile's own load: no
+                    // proxy fence), signalled on v_clean.
+                    if (!mbar_wait(&bars->v_full[zc % kVStages], (zc / kVStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sV = smem + kOffV + (zc % kVStages) * kTileBytes;
+                    const uint32_t bytes = (uint32_t)(kBN - ztail) * 128u;
+                    mbar_arrive_expect_tx(&bars->v_clean, 2 * bytes);
+                    bulk_load(sV + ztail * 128, g_zero_rows, bytes, &bars->v_clean);
+                    bulk_load(sV + kHalf + ztail * 128, g_zero_rows, bytes, &bars->v_clean);
+                }
             }
             if (!ok) record_failure(bars, p.err_count);
         }
@@ -473,6 +500,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         bool ok = true;
         int qcnt = 0, kcnt = 0, vcnt = 0;        // tiles consumed so far
         int pcnt[kQTiles] = {0, 0}, ocnt[kQTiles] = {0, 0};
+        int ccnt = 0;                             // v_clean phases consumed
         for (int n = 0; ok; ++n) {
             if (!wait_item(bars, n)) {
                 ok = false;
@@ -538,18 +566,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (ok && j == 0 && ocnt[a] >= 1)     // epilogue of the previous item done
                     ok = wait_all(&bars->o_empty[a], (ocnt[a] - 1) & 1);
                 if (kPaged && ok && zero_from >= 0 && j == it.n_kv - 1 && !tail_cleared) {
+                    // The producer zeroes the last tile's rows past Lk; the first
+                    // PV to read the tile waits for that (before P, to keep the
+                    // round trip off the softmax -> PV chain).
                     tail_cleared = true;
-                    // Cache rows past Lk in the last tile may hold any bits;
-                    // their probability is zero but 0 * NaN is not, so clear
-                    // them before the first PV reads the tile.
-                    uint8_t *sV = smem + kOffV + ((vbase + j) % kVStages) * kTileBytes;
-                    for (int idx = zero_from * 8 + lane; idx < kBN * 8; idx += 32) {
-                        const int r = idx >> 3, c = idx & 7;
-                        *reinterpret_cast<uint4 *>(sV + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(sV + kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                    ok = wait_all(&bars->v_clean, ccnt & 1);
+                    ++ccnt;
                 }
                 if (ok) ok = wait_all(&bars->p_full[a], pcnt[a] & 1);
                 if (!ok) return;
