@@ -21,11 +21,12 @@
 //    before V lands).  Every tile is stored as two 128-byte-swizzled halves
 //    of head_dim, the canonical layout tcgen05 reads.
 //  - Warp 9 allocates all 512 TMEM columns (S_a at 128a, O_a at 256 + 128a
-//    for query tile a) and one of its threads issues tcgen05.mma:
-//    S_a,j = Q_a K_j^T (M = N = 128, bf16 in, fp32 accumulate in TMEM), then
-//    O_a += P_a,j V_j with P read from tensor memory and V MN-major from
-//    shared memory.  The order PV_0,j, S_0,j+1, PV_1,j, S_1,j+1 lets one
-//    softmax warpgroup work while the tensor core serves the other.
+//    for query tile a).  Warps 9 and 10 issue tcgen05.mma for query tiles 0
+//    and 1: S_a,j = Q_a K_j^T (M = N = 128, bf16 in, fp32 accumulate in
+//    TMEM), then O_a += P_a,j V_j with P read from tensor memory and V
+//    MN-major from shared memory.  Each issues its tile's PV as soon as that
+//    tile's P is ready, so one softmax warpgroup works while the tensor core
+//    serves the other, in whatever order they finish.
 //  - Warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1:
 //    one row per thread (TMEM lane = row).  tcgen05.ld of the S row, causal
 //    mask on the diagonal tile (an unmasked tile's row max comes from the
@@ -60,13 +61,13 @@ constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kSoftmaxWarps = 4 * kQTiles;
 constexpr int kTmaWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kPrefillThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kMmaWarp = kSoftmaxWarps + 1;     // MMA warp of query tile a: kMmaWarp + a
+constexpr int kPrefillThreads = 32 * (kSoftmaxWarps + 1 + kQTiles);
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;      // S_a at kColS + 128a, O_a at kColO + 128a
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
 constexpr int kItemRing = 4;                    // item numbers in flight between the roles
-constexpr int kItemReaders = 1 + kQTiles * 4;   // the MMA warp and every softmax warp
+constexpr int kItemReaders = kQTiles * 5;       // the MMA warps and every softmax warp
 
 // One unit of work: a pair of 128-row query tiles of one head of one
 // sequence.  Items are numbered heaviest first (pair index descending, then
@@ -87,7 +88,9 @@ struct Barriers {
     uint64_t k_empty[kKStages], v_empty[kVStages];
     uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles], o_empty[kQTiles];
     uint64_t item_full[kItemRing], item_empty[kItemRing];
-    uint64_t v_clean;           // paged: the last V tile's rows past Lk are zeroed
+    // Paged: one phase per load into V slot s, completed at the load's issue,
+    // or for an item's last tile with rows past Lk once they are zeroed.
+    uint64_t v_clean[kVStages];
     Item item[kItemRing];       // decoded items; n_kv < 0 = no more work
     uint32_t tmem_base;
     int failed;
@@ -321,15 +324,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     Barriers *bars = reinterpret_cast<Barriers *>(smem + kOffBar);
 
     if (threadIdx.x == 0) {
+        // Q and every K / V tile are released once by each MMA warp: after
+        // its MMAs read it, or, if its query tile does not read it, as soon
+        // as it has seen the tile land.
         mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->q_empty, 1);
+        mbar_init(&bars->q_empty, kQTiles);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->k_empty[s], kQTiles);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->v_empty[s], 1);
+            mbar_init(&bars->v_empty[s], kQTiles);
         }
         for (int a = 0; a < kQTiles; ++a) {
             mbar_init(&bars->s_full[a], 1);
@@ -341,7 +347,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&bars->item_full[r], 1);
             mbar_init(&bars->item_empty[r], kItemReaders);
         }
-        mbar_init(&bars->v_clean, 1);
+        for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_clean[s], 1);
         bars->failed = 0;
         fence_mbarrier_init();
     }
@@ -403,6 +409,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     return false;
                 mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
                 load_tile(&v_map, smem + kOffV + st * kTileBytes, &bars->v_full[st], it, j);
+                if (kPaged && !(j == it.n_kv - 1 && it.Lk - j * kBN < kBN))
+                    mbar_arrive(&bars->v_clean[st]);      // nothing to zero in this tile
                 ++vcnt;
                 return true;
             };
@@ -480,17 +488,23 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                     uint8_t *sV = smem + kOffV + (zc % kVStages) * kTileBytes;
                     const uint32_t bytes = (uint32_t)(kBN - ztail) * 128u;
-                    mbar_arrive_expect_tx(&bars->v_clean, 2 * bytes);
-                    bulk_load(sV + ztail * 128, g_zero_rows, bytes, &bars->v_clean);
-                    bulk_load(sV + kHalf + ztail * 128, g_zero_rows, bytes, &bars->v_clean);
+                    uint64_t *vc = &bars->v_clean[zc % kVStages];
+                    mbar_arrive_expect_tx(vc, 2 * bytes);
+                    bulk_load(sV + ztail * 128, g_zero_rows, bytes, vc);
+                    bulk_load(sV + kHalf + ztail * 128, g_zero_rows, bytes, vc);
                 }
             }
             if (!ok) record_failure(bars, p.err_count);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp >= kMmaWarp) {
         // ------------------------------------------------------------- MMA
+        // One issuing warp per query tile, so each tile's PV and next QK^T go
+        // to the tensor core as soon as its own P is ready, whatever the other
+        // tile is doing (a single issuer has to serve the tiles in a fixed
+        // order and sits in one tile's waits while the other's P is ready).
         // The whole warp runs this loop (uniform control flow); elect.sync
         // inside each tcgen05 instruction picks the issuing lane.
+        const int a = warp - kMmaWarp;
         constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
         constexpr uint32_t kIdescPV = idesc_bf16(kBM, 128, true);
         // Waits are taken by every lane; the shuffle keeps `ok` uniform.
@@ -499,28 +513,30 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         };
         bool ok = true;
         int qcnt = 0, kcnt = 0, vcnt = 0;        // tiles consumed so far
-        int pcnt[kQTiles] = {0, 0}, ocnt[kQTiles] = {0, 0};
-        int ccnt = 0;                             // v_clean phases consumed
+        int pcnt = 0, ocnt = 0;
         for (int n = 0; ok; ++n) {
             if (!wait_item(bars, n)) {
                 ok = false;
                 break;
             }
-            // A private copy: every field stays in registers on the issue path
+            // The few fields this warp needs, in registers for the issue path
             // (a reference would be reloaded from shared memory after each wait).
-            const Item it = bars->item[n % kItemRing];
-            if (it.n_kv < 0) break;
-            const bool has1 = it.last[1] >= 0;
-            ok = wait_all(&bars->q_full, qcnt & 1);
-            ++qcnt;
+            const Item &itr = bars->item[n % kItemRing];
+            const int n_kv = itr.n_kv;
+            if (n_kv < 0) break;
+            const int last1 = itr.last[1];
+            // (a select, not itr.last[a]: one load either way)
+            const int last = a ? last1 : itr.last[0];
+            const int Lk = itr.Lk;
+            const bool has1 = last1 >= 0;
             // Key tile j of this item is ring slot kbase + j (same for V).
             const int kbase = kcnt, vbase = vcnt;
+            kcnt += n_kv;
+            vcnt += n_kv;
             // Paged: first row past Lk in the item's last key tile (-1: none).
-            const int tail = it.Lk - (it.n_kv - 1) * kBN;
+            const int tail = Lk - (n_kv - 1) * kBN;
             const int zero_from = (kPaged && tail < kBN) ? tail : -1;
-            bool tail_cleared = false;
             int k_ready = -1, v_ready = -1;
-            int s_left = (it.last[0] + 1) + (has1 ? it.last[1] + 1 : 0);
             auto ensure_k = [&](int j) {
                 if (ok && k_ready < j) {
                     const int c = kbase + j;
@@ -535,12 +551,35 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     v_ready = j;
                 }
             };
+            // Each warp sees every phase of q_full, k_full and v_full in order
+            // and releases a slot only after it has seen it filled, so no
+            // phase can complete twice before a warp's parity wait for it (a
+            // parity wait is sound only once the previous phase has completed).
+            // A tile this warp does not read is waited for and released at once.
+            auto pass_tile = [&](int j) {
+                ensure_k(j);
+                ensure_v(j);
+                __syncwarp();
+                if (ok && lane == 0) {
+                    mbar_arrive(&bars->k_empty[(kbase + j) % kKStages]);
+                    mbar_arrive(&bars->v_empty[(vbase + j) % kVStages]);
+                }
+            };
+            ok = wait_all(&bars->q_full, qcnt & 1);
+            ++qcnt;
+            if (a == 1 && !has1) {               // no second query tile
+                __syncwarp();
+                if (ok && lane == 0) mbar_arrive(&bars->q_empty);
+                for (int j = 0; ok && j < n_kv; ++j) pass_tile(j);
+                release_item(bars, n, lane);
+                continue;
+            }
             // Descriptors are built once per operand tile; each K=16 step only
             // adds a compile-time offset to the start-address field (shared
             // addresses are < 256 KB, so that 14-bit field never carries).
             // Rebuilding them per instruction costs the issuing warp ~30 cycles
             // per MMA, about half the tensor core's 64.
-            auto issue_s = [&](int a, int j) {
+            auto issue_s = [&](int j) {
                 ensure_k(j);
                 if (!ok) return;
                 tc_fence_after();
@@ -554,28 +593,28 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     tc_mma_elect(d, dq + off, dk + off, kIdescQK, kk > 0);
                 }
                 tc_commit_elect(&bars->s_full[a]);
-                // After the item's last QK^T the Q buffer may be refilled.
-                if (--s_left == 0) tc_commit_elect(&bars->q_empty);
+                // This warp's hold on K_j, and after its last QK^T on the Q
+                // buffers, ends when these MMAs have read them.
+                tc_commit_elect(&bars->k_empty[(kbase + j) % kKStages]);
+                if (j == last) tc_commit_elect(&bars->q_empty);
             };
-            auto issue_pv = [&](int a, int j) {
+            auto issue_pv = [&](int j) {
                 // V_j (and K_j+1 for the S that follows) were loaded long ago;
                 // confirm them before waiting for P so that these barrier round
                 // trips stay off the softmax -> PV -> S critical path.
                 ensure_v(j);
-                if (j + 1 <= it.last[a]) ensure_k(j + 1);
-                if (ok && j == 0 && ocnt[a] >= 1)     // epilogue of the previous item done
-                    ok = wait_all(&bars->o_empty[a], (ocnt[a] - 1) & 1);
-                if (kPaged && ok && zero_from >= 0 && j == it.n_kv - 1 && !tail_cleared) {
-                    // The producer zeroes the last tile's rows past Lk; the first
-                    // PV to read the tile waits for that (before P, to keep the
+                if (j + 1 <= last) ensure_k(j + 1);
+                if (ok && j == 0 && ocnt >= 1)        // epilogue of the previous item done
+                    ok = wait_all(&bars->o_empty[a], (ocnt - 1) & 1);
+                if (kPaged && ok && zero_from >= 0 && j == n_kv - 1)
+                    // The producer zeroes the last tile's rows past Lk; a PV
+                    // reading the tile waits for that (before P, to keep the
                     // round trip off the softmax -> PV chain).
-                    tail_cleared = true;
-                    ok = wait_all(&bars->v_clean, ccnt & 1);
-                    ++ccnt;
-                }
-                if (ok) ok = wait_all(&bars->p_full[a], pcnt[a] & 1);
+                    ok = wait_all(&bars->v_clean[(vbase + j) % kVStages],
+                                  ((vbase + j) / kVStages) & 1);
+                if (ok) ok = wait_all(&bars->p_full[a], pcnt & 1);
                 if (!ok) return;
-                ++pcnt[a];
+                ++pcnt;
                 tc_fence_after();
                 // P: 16 keys = 8 packed TMEM columns per step.  V: MN-major; 16
                 // keys = 2 swizzle atoms (2048 B) per step, the second 64 dims
@@ -587,28 +626,20 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_tmem_a_elect(d, pa + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4),
                                         kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-            };
-            issue_s(0, 0);
-            if (has1) issue_s(1, 0);
-            if (ok) tc_commit_elect(&bars->k_empty[kbase % kKStages]);
-            for (int j = 0; ok && j < it.n_kv; ++j) {
-                for (int a = 0; a < kQTiles && ok; ++a) {
-                    if (j > it.last[a]) continue;
-                    issue_pv(a, j);
-                    if (!ok) break;
-                    if (j == it.last[a]) {
-                        tc_commit_elect(&bars->o_full[a]);
-                        ++ocnt[a];
-                    } else {
-                        issue_s(a, j + 1);
-                    }
-                }
-                if (!ok) break;
                 tc_commit_elect(&bars->v_empty[(vbase + j) % kVStages]);
-                if (j + 1 < it.n_kv) tc_commit_elect(&bars->k_empty[(kbase + j + 1) % kKStages]);
+            };
+            issue_s(0);
+            for (int j = 0; ok && j <= last; ++j) {
+                issue_pv(j);
+                if (!ok) break;
+                if (j == last) {
+                    tc_commit_elect(&bars->o_full[a]);
+                    ++ocnt;
+                } else {
+                    issue_s(j + 1);
+                }
             }
-            kcnt += it.n_kv;
-            vcnt += it.n_kv;
+            for (int j = last + 1; ok && j < n_kv; ++j) pass_tile(j);   // tile 1's only
             release_item(bars, n, lane);
         }
         if (!ok && lane == 0) record_failure(bars, p.err_count);
