@@ -100,14 +100,39 @@ struct Barriers {
 // 64-dim half: at most 127 rows of 128 bytes).
 __device__ __align__(128) uint8_t g_zero_rows[kHalf];
 
+// The work list: every non-empty (query-tile pair, sequence), heaviest first.
+// Numbering every (pair, sequence, head) up to the longest sequence leaves
+// most early numbers empty (short sequences have no high pairs), and each
+// empty number costs the producer a round trip to the work counter; the
+// pair index is also only a proxy for the work when sequences carry a
+// cached prefix.  Each CTA therefore lists the (pair, sequence) entries in
+// shared memory and sorts them (bitonic) by the number of 128-key tiles the
+// pair's last row reads, most first, then by sequence and pair, so that every
+// CTA holds the same order; entry t, head h is item t * Hq + h.  Entry key:
+// (511 - min(tiles - 1, 511)) << 22 | sequence << 10 | pair.
+constexpr int kSchedMaxEntries = 4096, kSchedMaxSeqs = 4096, kSchedMaxPairs = 1024;
+struct Sched {
+    uint32_t key[kSchedMaxEntries];
+    int entries;
+    int fill;
+    int compact;                         // 0: the list is not used (too long)
+};
+
 // Returns false for an item with no rows; *bad is set when the sequence is
 // malformed (Lk < Lq), in which case no role touches it.
-__device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n_pairs, Item &it,
-                                            bool *bad = nullptr) {
+__device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n_pairs,
+                                            const Sched *sch, Item &it, bool *bad = nullptr) {
     const int h = w % p.Hq;
     const int t = w / p.Hq;
-    const int b = t % p.B;
-    const int pair = n_pairs - 1 - t / p.B;
+    int b, pair;
+    if (sch->compact) {
+        const uint32_t e = sch->key[t];
+        pair = (int)(e & 1023u);
+        b = (int)((e >> 10) & 4095u);
+    } else {
+        b = t % p.B;
+        pair = n_pairs - 1 - t / p.B;
+    }
     const int q_start = __ldg(p.cu_seqlens_q + b);
     const int L = __ldg(p.cu_seqlens_q + b + 1) - q_start;
     const int q0 = pair * kQTiles * kBM;
@@ -146,7 +171,8 @@ __device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n
     return true;
 }
 
-constexpr int kPrefillSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
+constexpr int kOffSched = (kOffBar + (int)sizeof(Barriers) + 15) / 16 * 16;
+constexpr int kPrefillSmemBytes = kOffSched + (int)sizeof(Sched) + 1024;
 
 // ------------------------------------------------------------ tcgen05 PTX
 __device__ __forceinline__ void tc_fence_before() {
@@ -322,6 +348,78 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Barriers *bars = reinterpret_cast<Barriers *>(smem + kOffBar);
+    Sched *sch = reinterpret_cast<Sched *>(smem + kOffSched);
+
+    // ---- the work list (see Sched); every thread takes part.
+    {
+        const int B = p.B;
+        const int tid = threadIdx.x;
+        // Pair count of sequence b, and the key tiles pair `pr` of it reads
+        // (a malformed sequence counts 1; decode_item flags it).
+        auto seq_pairs = [&](int b, int &L, int &Lk) {
+            const int qs = __ldg(p.cu_seqlens_q + b);
+            L = __ldg(p.cu_seqlens_q + b + 1) - qs;
+            const int ks = __ldg(p.cu_seqlens_k + b);
+            Lk = __ldg(p.cu_seqlens_k + b + 1) - ks;
+            const int np = L > 0 ? (L + kQTiles * kBM - 1) / (kQTiles * kBM) : 0;
+            return np < n_pairs ? np : n_pairs;
+        };
+        auto tiles_of = [&](int pr, int L, int Lk) {
+            if (Lk < L || Lk <= 0) return 1;
+            const int last_row = min(L, (pr + 1) * kQTiles * kBM) - 1;
+            const int t = (Lk - L + last_row) / kBN + 1;
+            return t < 1 ? 1 : (t > 512 ? 512 : t);
+        };
+        bool compact = B <= kSchedMaxSeqs && n_pairs <= kSchedMaxPairs;
+        if (tid == 0) {
+            sch->entries = 0;
+            sch->fill = 0;
+        }
+        __syncthreads();
+        if (compact) {
+            for (int b = tid; b < B; b += kPrefillThreads) {
+                int L, Lk;
+                const int np = seq_pairs(b, L, Lk);
+                if (np > 0) atomicAdd(&sch->entries, np);
+            }
+        }
+        __syncthreads();
+        const int E = sch->entries;
+        compact = compact && E <= kSchedMaxEntries;
+        if (compact) {
+            int N = 1;
+            while (N < E) N <<= 1;
+            for (int b = tid; b < B; b += kPrefillThreads) {
+                int L, Lk;
+                const int np = seq_pairs(b, L, Lk);
+                if (np == 0) continue;
+                const int at = atomicAdd(&sch->fill, np);
+                for (int pr = 0; pr < np; ++pr)
+                    sch->key[at + pr] = (uint32_t)(511 - (tiles_of(pr, L, Lk) - 1)) << 22 |
+                                        (uint32_t)b << 10 | (uint32_t)pr;
+            }
+            for (int i = E + tid; i < N; i += kPrefillThreads) sch->key[i] = 0xFFFFFFFFu;
+            __syncthreads();
+            for (int k = 2; k <= N; k <<= 1) {
+                for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                    for (int i = tid; i < N; i += kPrefillThreads) {
+                        const int ixj = i ^ jj;
+                        if (ixj > i) {
+                            const uint32_t x = sch->key[i], y = sch->key[ixj];
+                            if ((x > y) == ((i & k) == 0)) {
+                                sch->key[i] = y;
+                                sch->key[ixj] = x;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+        }
+        if (tid == 0) sch->compact = compact ? 1 : 0;
+        __syncthreads();
+        if (sch->compact) n_items = E * p.Hq;
+    }
 
     if (threadIdx.x == 0) {
         // Q and every K / V tile are released once by each MMA warp: after
@@ -432,7 +530,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         return;
                     }
                     bool bad = false;
-                    if (decode_item(w, p, n_pairs, it, &bad)) return;
+                    if (decode_item(w, p, n_pairs, sch, it, &bad)) return;
                     if (bad) count_error(p.err_count);
                 }
             };
