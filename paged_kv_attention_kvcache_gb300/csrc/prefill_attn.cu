@@ -779,6 +779,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 // iff c <= vis); the others pay nothing.
                 const bool diag = kOffset ? j >= mask_from : j == last;
                 const int vis = kOffset ? vis_row - j * kBN : row;
+                // The warp's lanes are consecutive rows: the range of their vis.
+                const int vis_lo = __shfl_sync(0xffffffffu, vis, 0);
+                const int vis_hi = __shfl_sync(0xffffffffu, vis, 31);
                 float mx4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
@@ -790,18 +793,48 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     // Tie the maxima to the wait so no use is scheduled above it.
                     asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
                 } else {
-                    // Masked: the next chunk's load is in flight while this one is reduced.
-                    uint32_t rb[2][32];
-                    tmem_ld32(lane_addr + col_s, rb[0]);
-                    tmem_wait_ld();
+                    if constexpr (kOffset) {
+                        // Masked, with a key offset (masked tiles are common): the
+                        // warp's rows see keys up to vis_lo .. vis_hi (lanes are
+                        // consecutive rows), so each 32-column chunk is visible to every
+                        // lane (reduced by the load), to none (skipped), or to some
+                        // (reduced under the mask).  The plain prefill's one diagonal
+                        // tile per query tile keeps the uniform pipelined loop below:
+                        // the split made its warps uneven and measured slower there.
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
-                        const uint32_t (&r)[32] = rb[c & 1];
+                        for (int c = 0; c < 4; ++c) {
+                            if (c * 32 + 31 <= vis_lo) {
+                                mx4[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
+                            } else if (c * 32 <= vis_hi) {
+                                uint32_t r[32];
+                                tmem_ld32(lane_addr + col_s + c * 32, r);
+                                tmem_wait_ld();
+                                float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (c * 32 + e <= vis) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(r[e]));
-                        if (c < 3) tmem_wait_ld();
+                                for (int e = 0; e < 16; ++e) {
+                                    const float x0 = c * 32 + 2 * e <= vis ? __uint_as_float(r[2 * e]) : -INFINITY;
+                                    const float x1 = c * 32 + 2 * e + 1 <= vis ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
+                                    m2[e & 1] = fmax3(m2[e & 1], x0, x1);
+                                }
+                                mx4[c] = fmaxf(m2[0], m2[1]);
+                            }
+                        }
+                        tmem_wait_ld();
+                        asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
+                    } else {
+                        // Masked: the next chunk's load is in flight while this one is reduced.
+                        uint32_t rb[2][32];
+                        tmem_ld32(lane_addr + col_s, rb[0]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                            const uint32_t (&r)[32] = rb[c & 1];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (c * 32 + e <= vis) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(r[e]));
+                            if (c < 3) tmem_wait_ld();
+                        }
                     }
                 }
                 const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
@@ -855,24 +888,62 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                         tmem_st16(lane_addr + col_s + c * 16, pk);
                     }
                 } else {
-                    uint32_t rb[2][32];
-                    tmem_ld32(lane_addr + col_s, rb[0]);
-                    tmem_wait_ld();
+                    if constexpr (kOffset) {
+                        // Chunks as in pass 1: invisible ones get P = 0 without a load,
+                        // fully visible ones the unmasked arithmetic.  Chunk c's P
+                        // columns lie in chunk c / 2's scores, read at step c / 2 <= c.
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
-                        const uint32_t (&r)[32] = rb[c & 1];
-                        uint32_t pk[16];
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t pk[16];
+                            if (c * 32 > vis_hi) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int k0 = c * 32 + 2 * e;
-                            const float p0 = k0 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
-                            const float p1 = k0 + 1 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
-                            sum4[e & 3] += p0 + p1;
-                            pk[e] = pack_bf16x2(p0, p1);
+                                for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                            } else {
+                                uint32_t r[32];
+                                tmem_ld32(lane_addr + col_s + c * 32, r);
+                                tmem_wait_ld();
+                                if (c * 32 + 31 <= vis_lo) {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) {
+                                        const float2 x = ffma2(__uint_as_float(r[2 * e]),
+                                                               __uint_as_float(r[2 * e + 1]), sl2, neg_m);
+                                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                                        sum2[e & 1] = fadd2(sum2[e & 1], pp);
+                                        pk[e] = pack_bf16x2(pp.x, pp.y);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) {
+                                        const int k0 = c * 32 + 2 * e;
+                                        const float p0 = k0 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
+                                        const float p1 = k0 + 1 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
+                                        sum4[e & 3] += p0 + p1;
+                                        pk[e] = pack_bf16x2(p0, p1);
+                                    }
+                                }
+                            }
+                            tmem_st16(lane_addr + col_s + c * 16, pk);
                         }
-                        if (c < 3) tmem_wait_ld();
-                        tmem_st16(lane_addr + col_s + c * 16, pk);
+                    } else {
+                        uint32_t rb[2][32];
+                        tmem_ld32(lane_addr + col_s, rb[0]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                            const uint32_t (&r)[32] = rb[c & 1];
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int k0 = c * 32 + 2 * e;
+                                const float p0 = k0 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
+                                const float p1 = k0 + 1 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
+                                sum4[e & 3] += p0 + p1;
+                                pk[e] = pack_bf16x2(p0, p1);
+                            }
+                            if (c < 3) tmem_wait_ld();
+                            tmem_st16(lane_addr + col_s + c * 16, pk);
+                        }
                     }
                 }
                 tmem_wait_st();

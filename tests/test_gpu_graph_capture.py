@@ -107,7 +107,10 @@ def test_prefill_side_entry_points_replay_from_a_graph():
     vb = qkv0[:, Q + D:].reshape(T, s.hkv, 128)
     ref = oracle.attention_varlen(qb, kb, vb, cu, cu, SCALE, True)
     check_close(eager[5], ref, "graph-captured prefill")
-    assert np.array_equal(eager[5], eager[6]), "paged and contiguous prefill agree bit for bit"
+    # The paged call runs the key-offset kernel (its masked tiles split into
+    # visible / partial / invisible chunks), the contiguous one with one
+    # cu_seqlens array the plain kernel: both within the oracle's tolerance.
+    check_close(eager[6], ref, "graph-captured paged prefill")
 
 
 def test_noalloc_decode_replays_from_a_graph():
