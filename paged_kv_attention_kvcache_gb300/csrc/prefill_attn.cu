@@ -241,7 +241,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // The maximum of the thread's 32 fp32 columns, reduced by the load itself
 // (tcgen05.ld.red, sm_103a).  The loaded values are not used.
 __device__ __forceinline__ float tmem_ld32_max(uint32_t taddr) {
-    uint32_t r[32];
+    [[maybe_unused]] uint32_t r[32];
     float mx;
     asm volatile(
         "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
@@ -465,6 +465,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             tma_prefetch_desc(&q_map);
             tma_prefetch_desc(&k_map);
             tma_prefetch_desc(&v_map);
+            // Q tiles are read by one item only: evict them from L2 first, so
+            // K/V tiles (re-read by the other heads of their kv group) stay.
+            const uint64_t pol_first = l2_policy_evict_first();
             int qcnt = 0, kcnt = 0, vcnt = 0;
             bool ok = true;
             // K runs one tile ahead of V, so QK^T of the next tile never waits
@@ -557,8 +560,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 for (int a = 0; a < (has1 ? 2 : 1); ++a) {
                     uint8_t *sQ = smem + kOffQ + a * kTileBytes;
                     const int row = it.q_start + it.q0 + a * kBM;
-                    tma_load_3d(sQ, &q_map, &bars->q_full, 0, it.h, row);
-                    tma_load_3d(sQ + kHalf, &q_map, &bars->q_full, 64, it.h, row);
+                    tma_load_3d_hint(sQ, &q_map, &bars->q_full, 0, it.h, row, pol_first);
+                    tma_load_3d_hint(sQ + kHalf, &q_map, &bars->q_full, 64, it.h, row, pol_first);
                 }
                 ++qcnt;
                 ok = load_k(it, 0);
@@ -963,6 +966,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const int qpos = it.q0 + a * kBM + row;
             const float inv_l = 1.f / l;
             uint16_t *orow = p.o + ((int64_t)(it.q_start + qpos) * p.Hq + it.h) * 128;
+            const bool o_aligned32 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
             uint32_t rb[2][32];
             tmem_ld32(lane_addr + col_o, rb[0]);
             tmem_wait_ld();
@@ -971,14 +975,23 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (c < 3) tmem_ld32(lane_addr + col_o + (c + 1) * 32, rb[(c + 1) & 1]);
                 const uint32_t (&r)[32] = rb[c & 1];
                 if (qpos < it.L) {
+                    uint32_t w[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[8 * e]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
-                        *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) = v;
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                    if (o_aligned32) {
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2)
+                            asm volatile("st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                                         :: "l"(orow + c * 32 + 16 * h2), "r"(w[8 * h2]), "r"(w[8 * h2 + 1]),
+                                            "r"(w[8 * h2 + 2]), "r"(w[8 * h2 + 3]), "r"(w[8 * h2 + 4]),
+                                            "r"(w[8 * h2 + 5]), "r"(w[8 * h2 + 6]), "r"(w[8 * h2 + 7])
+                                         : "memory");
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4 *>(orow + c * 32 + 8 * e) =
+                                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                     }
                 }
                 if (c < 3) tmem_wait_ld();
