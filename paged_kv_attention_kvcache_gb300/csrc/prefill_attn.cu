@@ -834,8 +834,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                             if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
                             const uint32_t (&r)[32] = rb[c & 1];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (c * 32 + e <= vis) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(r[e]));
+                            for (int e = 0; e < 16; ++e) {
+                                const float x0 = c * 32 + 2 * e <= vis ? __uint_as_float(r[2 * e]) : -INFINITY;
+                                const float x1 = c * 32 + 2 * e + 1 <= vis ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
+                                mx4[e & 3] = fmax3(mx4[e & 3], x0, x1);
+                            }
                             if (c < 3) tmem_wait_ld();
                         }
                     }
@@ -865,7 +868,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 // written over the first 64 columns of S.  Chunk c's P columns
                 // [16c, 16c + 16) lie below its S columns [32c, 32c + 32), so a
                 // later chunk's scores are never overwritten before they are read.
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
                 float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 const float neg_m = -m_used;
                 if (!diag) {
@@ -918,10 +920,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                                     for (int e = 0; e < 16; ++e) {
                                         const int k0 = c * 32 + 2 * e;
-                                        const float p0 = k0 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
-                                        const float p1 = k0 + 1 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
-                                        sum4[e & 3] += p0 + p1;
-                                        pk[e] = pack_bf16x2(p0, p1);
+                                        float2 x = ffma2(__uint_as_float(r[2 * e]),
+                                                         __uint_as_float(r[2 * e + 1]), sl2, neg_m);
+                                        x.x = k0 <= vis ? x.x : -INFINITY;      // 2^-inf = 0
+                                        x.y = k0 + 1 <= vis ? x.y : -INFINITY;
+                                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                                        sum2[e & 1] = fadd2(sum2[e & 1], pp);
+                                        pk[e] = pack_bf16x2(pp.x, pp.y);
                                     }
                                 }
                             }
@@ -939,10 +944,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int k0 = c * 32 + 2 * e;
-                                const float p0 = k0 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m)) : 0.f;
-                                const float p1 = k0 + 1 <= vis ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m)) : 0.f;
-                                sum4[e & 3] += p0 + p1;
-                                pk[e] = pack_bf16x2(p0, p1);
+                                float2 x = ffma2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]),
+                                                 sl2, neg_m);
+                                x.x = k0 <= vis ? x.x : -INFINITY;      // 2^-inf = 0
+                                x.y = k0 + 1 <= vis ? x.y : -INFINITY;
+                                const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                                sum2[e & 1] = fadd2(sum2[e & 1], pp);
+                                pk[e] = pack_bf16x2(pp.x, pp.y);
                             }
                             if (c < 3) tmem_wait_ld();
                             tmem_st16(lane_addr + col_s + c * 16, pk);
@@ -950,8 +958,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                 }
                 tmem_wait_st();
-                l = fmaf(l, alpha, ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3])) +
-                                       ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)));
+                l = fmaf(l, alpha, (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->p_full[a]);
