@@ -49,7 +49,7 @@ DECODE_TRAFFIC = {"ratio": 1.0037, "source_sha256_16": "6069696183c8d8aa"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1054846464, "source_sha256_16": "21e6c16185b04063"}
+PREFILL_TRAFFIC = {"bytes": 1056627072, "source_sha256_16": "1f11638ef4859df8"}
 
 
 def max_over_ranks(values, world: int, device=None):
