@@ -358,11 +358,28 @@ int decode_resolve_split(int B, int Hkv, int max_blocks, int block_size, int kv_
     if (kv_split_tokens > 0) {
         split = (kv_split_tokens + kTile - 1) / kTile * kTile;
     } else {
-        // Enough CTAs for several waves of two CTAs per SM, but splits no
-        // shorter than 256 keys (each split pays a pipeline fill).
-        split = 1024;
-        const int64_t target = 8LL * num_sms;
-        while (split > 256 && (int64_t)B * Hkv * ((max_ctx + split - 1) / split) < target) split /= 2;
+        // Each split pays a fixed cost (pipeline fill, its partial result and
+        // its share of the merge), so long splits win while the grid still
+        // balances: the longest of 4096 .. 1536 keys that leaves the longest
+        // context at least four splits and the grid twelve CTAs per SM.
+        // (Measured on GB300 against fixed splits: the best or within 1% on
+        // B = 64 x 4k, 256 x 8k and 32 x 40k contexts; 1024-key splits lost
+        // 5% on the last.)  Otherwise, enough CTAs for several waves of two
+        // CTAs per SM, with splits no shorter than 256 keys.
+        split = 0;
+        for (const int64_t cand : {4096, 3072, 2048, 1536}) {
+            if (4 * cand <= max_ctx &&
+                (int64_t)B * Hkv * ((max_ctx + cand - 1) / cand) >= 12LL * num_sms) {
+                split = cand;
+                break;
+            }
+        }
+        if (split == 0) {
+            split = 1024;
+            const int64_t target = 8LL * num_sms;
+            while (split > 256 && (int64_t)B * Hkv * ((max_ctx + split - 1) / split) < target)
+                split /= 2;
+        }
     }
     if (split > cap) split = cap;
     if (split < kTile) split = kTile;
