@@ -889,8 +889,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                             sum2[e & 1] = fadd2(sum2[e & 1], pp);
                             pk[e] = pack_bf16x2(pp.x, pp.y);
                         }
-                        if (c < 3) tmem_wait_ld();
+                        // P's columns are not the ones loading: store, then wait.
                         tmem_st16(lane_addr + col_s + c * 16, pk);
+                        if (c < 3) tmem_wait_ld();
                     }
                 } else {
                     if constexpr (kOffset) {
@@ -952,8 +953,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                                 sum2[e & 1] = fadd2(sum2[e & 1], pp);
                                 pk[e] = pack_bf16x2(pp.x, pp.y);
                             }
-                            if (c < 3) tmem_wait_ld();
                             tmem_st16(lane_addr + col_s + c * 16, pk);
+                            if (c < 3) tmem_wait_ld();
                         }
                     }
                 }
