@@ -53,7 +53,7 @@ DECODE_TRAFFIC = {"ratio": 1.0032, "source_sha256_16": "d3501388239b5f8d"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1052708352, "source_sha256_16": "59d84215ae77319a"}
+PREFILL_TRAFFIC = {"bytes": 1056003456, "source_sha256_16": "d0e6a9186311df04"}
 
 
 def max_over_ranks(values, world: int, device=None):
