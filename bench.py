@@ -48,12 +48,12 @@ SCALE = 128 ** -0.5
 # DRAM bytes per algorithmic byte of the decode attention kernels, from an
 # ncu capture of `bench.py --ncu-case decode` (reads + writes of
 # decode_split_kernel over its algorithmic bytes), valid only for the kernel
-# source it was taken on.
-DECODE_TRAFFIC = {"ratio": 1.0032, "source_sha256_16": "d3501388239b5f8d"}
+# code it was taken on (the hash ignores comments and layout).
+DECODE_TRAFFIC = {"ratio": 1.0032, "source_sha256_16": "c016c1bf02d2a4c9"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1056003456, "source_sha256_16": "d0e6a9186311df04"}
+PREFILL_TRAFFIC = {"bytes": 1056003456, "source_sha256_16": "3b39ece31c628a8d"}
 
 
 def max_over_ranks(values, world: int, device=None):
@@ -75,11 +75,38 @@ def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
     return world * units_per_rank / seconds
 
 
+def strip_comments(src: str) -> str:
+    """C/CUDA source without its comments, whitespace runs collapsed (string
+    and character literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(name: str) -> str:
+    """Hash of a kernel source's code: comments and layout do not count, so a
+    traffic figure taken on the code stays valid across comment edits."""
     import hashlib
     path = os.path.join(ROOT, "paged_kv_attention_kvcache_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path, encoding="utf-8") as f:
+        return hashlib.sha256(strip_comments(f.read()).encode()).hexdigest()[:16]
 
 
 def measured_peaks():

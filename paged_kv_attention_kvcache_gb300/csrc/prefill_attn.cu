@@ -11,15 +11,20 @@
 //  - Persistent: one CTA per SM walks work items, an item being a pair of
 //    adjacent 128-row query tiles of one query head of one sequence, so
 //    every K/V tile loaded serves 256 query rows.  Items are numbered
-//    heaviest first (most keys under the causal mask).  With a work counter
+//    heaviest first: each CTA sorts the non-empty (pair, sequence) entries by
+//    the number of key tiles the pair's last row reads (then sequence, then
+//    pair), and item t * Hq + h is entry t, head h.  With a work counter
 //    the TMA lane takes the next number from it (atomicAdd), so CTAs that
 //    drew light items take more of them; without one, CTA c takes items c,
 //    c + grid, ...  Either way the number is handed to the other warps
 //    through a small ring in shared memory.
-//  - Warp 8 issues TMA loads: both Q tiles once, then 128-token K and V
-//    tiles into two-deep rings (separate K and V barriers, so QK^T can start
-//    before V lands).  Every tile is stored as two 128-byte-swizzled halves
-//    of head_dim, the canonical layout tcgen05 reads.
+//  - Warp 8 issues TMA loads: both Q tiles once (L2 evict-first: no other
+//    item reads them), then 128-token K and V tiles into two-deep rings
+//    (separate K and V barriers, so QK^T can start before V lands).  Every
+//    tile is stored as two 128-byte-swizzled halves of head_dim, the
+//    canonical layout tcgen05 reads.  Paged: one block-table lookup per key
+//    tile, and the rows past Lk of an item's last V tile are overwritten
+//    with zeros once it lands (cache rows there may hold any bits).
 //  - Warp 9 allocates all 512 TMEM columns (S_a at 128a, O_a at 256 + 128a
 //    for query tile a).  Warps 9 and 10 issue tcgen05.mma for query tiles 0
 //    and 1: S_a,j = Q_a K_j^T (M = N = 128, bf16 in, fp32 accumulate in
@@ -37,8 +42,9 @@
 //    it.  The commit
 //    that signals S_a,j also covers PV_a,j-1 (issued before it), so a rescale
 //    of O_a after S_a,j has landed never races the tensor core.
-//  - Epilogue: O_a / l straight to global memory with predicated 16-byte
-//    stores (a TMA store cannot clip at sequence boundaries).
+//  - Epilogue: O_a / l straight to global memory with predicated 32-byte
+//    stores marked L2 evict-first (16-byte ones when o is only 16-byte
+//    aligned; a TMA store cannot clip at sequence boundaries).
 #include <math.h>
 
 #include "common.cuh"
@@ -70,8 +76,9 @@ constexpr int kItemRing = 4;                    // item numbers in flight betwee
 constexpr int kItemReaders = kQTiles * 5;       // the MMA warps and every softmax warp
 
 // One unit of work: a pair of 128-row query tiles of one head of one
-// sequence.  Items are numbered heaviest first (pair index descending, then
-// sequence, then head, so the heads sharing a kv head are adjacent).
+// sequence.  Items are numbered heaviest first (key tiles read, then
+// sequence, then pair, then head, so the heads sharing a kv head are
+// adjacent).
 // A sequence has Lq queries and Lk >= Lq keys; query i sits at key position
 // off + i with off = Lk - Lq (causality aligned to the last key: off = 0 for
 // a plain prefill, the cached prefix length for a prefix hit or a chunk).
