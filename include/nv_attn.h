@@ -203,6 +203,20 @@ NV_API int nv_qknorm_rope_store(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k
                                 int *err_count, void *stream);
 
 /*
+ * Failure-path self-test (no page counterpart: it checks this library's own
+ * stall reporting).  Launches one CTA whose thread waits on a shared-memory
+ * mbarrier that nothing arrives on, through the same bounded wait every
+ * pipeline here uses.  The wait gives up after about a second and sets
+ * NV_ERR_PIPELINE_FAILURE in *err_count, as a stalled pipeline would; the
+ * kernel then exits normally, so the context stays usable.  Later calls that
+ * are given the same err_count skip their work while the bit is set (clear
+ * it first).
+ *   err_count    one int the device can address (4-byte aligned), required.
+ * Returns NV_EINVAL for a null or misaligned err_count.
+ */
+NV_API int nv_selftest_wait_timeout(int *err_count, void *stream);
+
+/*
  * SiluAndMul, the SwiGLU activation of the MLP that follows the attention
  * sublayer.  "3.3 Model skeleton and core operators", sec. 4 (SwiGLU:
  * SiluAndMul splits the merged gate_up output in half along the last dim,

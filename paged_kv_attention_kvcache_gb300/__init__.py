@@ -27,14 +27,14 @@ __all__ = [
     "NvAttnError", "library", "library_path", "nv_version",
     "nv_rope_cos_sin_cache", "nv_add_rmsnorm", "nv_qknorm_rope", "nv_store_kvcache",
     "nv_qknorm_rope_store", "nv_prefill_attn_varlen", "nv_prefill_attn_paged", "nv_decode_attn_workspace_size",
-    "nv_decode_attn_paged", "nv_silu_and_mul", "ABI_FUNCTIONS",
+    "nv_decode_attn_paged", "nv_silu_and_mul", "nv_selftest_wait_timeout", "ABI_FUNCTIONS",
 ]
 
 ABI_FUNCTIONS = (
     "nv_status_string", "nv_version", "nv_rope_cos_sin_cache", "nv_add_rmsnorm",
     "nv_qknorm_rope", "nv_store_kvcache", "nv_qknorm_rope_store", "nv_prefill_attn_varlen",
     "nv_prefill_attn_paged", "nv_decode_attn_workspace_size", "nv_decode_attn_paged",
-    "nv_decode_attn_paged_noalloc", "nv_silu_and_mul",
+    "nv_decode_attn_paged_noalloc", "nv_silu_and_mul", "nv_selftest_wait_timeout",
 )
 
 _P, _I64, _I32, _F32, _F64, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -54,6 +54,7 @@ _SIGNATURES = {
     "nv_prefill_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _I64, _I32, _I32, _I32,
                                _I32, _I32, _I64, _F32, _I32, _P, _P, _P], _I32),
     "nv_silu_and_mul": ([_P, _I64, _P, _I64, _I64, _I32, _P], _I32),
+    "nv_selftest_wait_timeout": ([_P, _P], _I32),
     "nv_decode_attn_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "nv_decode_attn_paged": ([_P, _I64, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32,
                               _I64, _F32, _I32, _P, _SZ, _P, _P], _I32),
@@ -242,6 +243,13 @@ def nv_decode_attn_paged(q, k_cache, v_cache, block_tables, context_lens, o,
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), _ptr(o), B, Hq, Hkv, d, bs, nb, float(softmax_scale),
         int(kv_split_tokens), _ptr(workspace), ws_bytes, _ptr(err_count), _stream(stream)))
+
+
+def nv_selftest_wait_timeout(err_count, stream=None) -> None:
+    """One bounded wait that cannot succeed (about a second): sets
+    NV_ERR_PIPELINE_FAILURE (bit 30) in err_count, an int32 device tensor."""
+    _check("nv_selftest_wait_timeout", library().nv_selftest_wait_timeout(
+        _ptr(err_count), _stream(stream)))
 
 
 def nv_silu_and_mul(x, out, stream=None) -> None:

@@ -198,6 +198,11 @@ int nv_qknorm_rope_store(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k,
         write_k, err_count, as_stream(stream)));
 }
 
+int nv_selftest_wait_timeout(int *err_count, void *stream) {
+    if (!err_count || (uintptr_t)err_count % 4) return NV_EINVAL;
+    return launch_status(launch_wait_timeout_selftest(err_count, as_stream(stream)));
+}
+
 int nv_silu_and_mul(const nv_bf16_t *x, int64_t x_tok_stride, nv_bf16_t *out,
                     int64_t out_tok_stride, int64_t T, int intermediate, void *stream) {
     if (T < 0 || intermediate < 0) return NV_EINVAL;

@@ -64,6 +64,10 @@ cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
                                      int64_t T, int Hq, int Hkv, float eps, int write_k,
                                      int *err_count, cudaStream_t s);
 
+// One bounded mbarrier wait that cannot succeed (about a second); records
+// kPipelineFailureBit in err_count when it gives up.
+cudaError_t launch_wait_timeout_selftest(int *err_count, cudaStream_t s);
+
 cudaError_t launch_silu_and_mul(const uint16_t *x, int64_t x_stride, uint16_t *out,
                                 int64_t out_stride, int64_t T, int I, cudaStream_t s);
 

@@ -197,3 +197,9 @@ def test_silu_and_mul_rejects_bad_arguments(lib):
     assert f(X, 24576, X, 12288, 4, 12288, None) == NV_EINVAL      # same base, other stride
     assert f(X, 24576, O, 12288, 0, 12288, None) == NV_OK
     assert f(X, 24576, O, 12288, -1, 12288, None) == NV_EINVAL
+
+
+def test_wait_timeout_selftest_rejects_bad_counter(lib):
+    # Checked on the host before any launch.
+    assert lib.nv_selftest_wait_timeout(None, None) == NV_EINVAL
+    assert lib.nv_selftest_wait_timeout(MIS, None) == NV_EINVAL

@@ -128,3 +128,33 @@ def test_prefill_overstated_max_seqlen_is_safe():
     c = wl.cu_seqlens(lengths)
     check_close(host(o), oracle.attention_varlen(qb, kb, vb, c, c, SCALE, True),
                 "prefill with overstated max_seqlen")
+
+
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable():
+    # A wait on an mbarrier nothing arrives on (the pipelines' own bounded
+    # wait) gives up after about a second and sets bit 30 of err_count.
+    err = err_counter()
+    nv.nv_selftest_wait_timeout(err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & (1 << 30)
+    # Work given the flagged counter is skipped: o keeps its sentinel.
+    hq, hkv, lengths = 4, 2, np.array([200, 37])
+    T = int(lengths.sum())
+    q = wl.normal_bf16(970, "st.q", (T, hq, 128))
+    k = wl.normal_bf16(970, "st.k", (T, hkv, 128))
+    v = wl.normal_bf16(970, "st.v", (T, hkv, 128))
+    cu = wl.cu_seqlens(lengths)
+    o = torch.full((T, hq, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    nv.nv_prefill_attn_varlen(dev(q), dev(k), dev(v), o, dev_i32(cu), dev_i32(cu), 200, 200,
+                              SCALE, err_count=err)
+    torch.cuda.synchronize()
+    assert bool(torch.all(o == 7.0))
+    # The context is still usable: with a clear counter the same call runs and
+    # matches the oracle.
+    fresh = err_counter()
+    nv.nv_prefill_attn_varlen(dev(q), dev(k), dev(v), o, dev_i32(cu), dev_i32(cu), 200, 200,
+                              SCALE, err_count=fresh)
+    torch.cuda.synchronize()
+    assert int(fresh.item()) == 0
+    check_close(host(o), oracle.attention_varlen(q, k, v, cu, cu, SCALE, True),
+                "prefill after a reported stall")
