@@ -44,9 +44,9 @@
  *   - No entry point waits on another CTA.  Waits inside a CTA (its own
  *     copy and tensor-core pipeline) give up after about a second; the
  *     kernel then sets bit 30 (NV_ERR_PIPELINE_FAILURE) of err_count, leaves
- *     the affected outputs unwritten and finishes.  CTAs that start after
- *     the bit is set skip their work.  Only a defect can cause this; clear
- *     err_count before reusing it.
+ *     the affected outputs unwritten (decode writes NaN into them instead)
+ *     and finishes.  CTAs that start after the bit is set skip their work.
+ *     Only a defect can cause this; clear err_count before reusing it.
  *   - Calls are asynchronous and allocate nothing.
  *
  * Sources are cited by page title and section.
@@ -348,7 +348,8 @@ NV_API size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim
  *                 nv_decode_attn_workspace_size(...) bytes (may be NULL
  *                 when that size is 0); contents on entry are ignored.
  * A block id outside [0, num_blocks) or L > max_blocks_per_seq *
- * block_size is counted in err_count; the offending keys are skipped.
+ * block_size is counted in err_count; the offending keys are skipped: o is
+ * the attention over the keys that remain, zeros if none remain.
  * Requires head_dim == 128, block_size % 64 == 0, 1 <= G <= 16, 16-byte
  * aligned pointers, q_tok_stride a multiple of 8, B <= 65535.
  */
@@ -377,13 +378,18 @@ NV_API int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride,
  *     more than that (nv_decode_attn_workspace_size(...) with the same
  *     arguments tells in advance); use nv_decode_attn_paged, a larger
  *     kv_split_tokens, or fewer sequences per call.
+ *   - Arguments are checked exactly as nv_decode_attn_paged checks them,
+ *     with the same codes; NV_EWORKSPACE comes only for a call that is
+ *     otherwise valid.
  *   - The first call on each device looks up the array's device address
- *     with that device current; make that first call before any stream
- *     capture.
+ *     with that device current (and looks it up again when the device's
+ *     context has changed, e.g. after cudaDeviceReset); make that first call
+ *     before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents
- *     (nothing in it needs to start at zero).  Calls whose kernels overlap
- *     on the GPU -- on different streams, or from different threads --
- *     race on it; serialise them.
+ *     (nothing in it needs to start at zero: every slot the merge reads was
+ *     written by the same call, and after a pipeline failure the merge reads
+ *     none).  Calls whose kernels overlap on the GPU -- on different
+ *     streams, or from different threads -- race on it; serialise them.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define NV_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

@@ -83,6 +83,41 @@ bool make_tensor_map_bf16(CUtensorMap *map, const void *base, int rank, const ui
     return r == CUDA_SUCCESS;
 }
 
+int decode_check_args(const void *q, int64_t q_tok_stride, const void *k_cache,
+                      const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, const void *o, int B, int Hq, int Hkv,
+                      int head_dim, int block_size, int64_t num_blocks, float softmax_scale,
+                      int kv_split_tokens, DecodePlan *plan) {
+    plan->split_tokens = 0;
+    plan->max_splits = 0;
+    plan->workspace_bytes = 0;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || kv_split_tokens < 0 || !(softmax_scale > 0.f) ||
+        !isfinite(softmax_scale))
+        return NV_EINVAL;
+    if (head_dim != 128 || block_size % 64 != 0 || Hq / Hkv > 16 || B > 65535 || Hkv > 65535)
+        return NV_EUNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > 0x7FFFFFFF || num_blocks > 0x7FFFFFFF)
+        return NV_EUNSUPPORTED;
+    if (B == 0) return NV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !o) return NV_EINVAL;
+    if (q_tok_stride < (int64_t)Hq * 128) return NV_EINVAL;
+    if (q_tok_stride % 8 || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(o))
+        return NV_EALIGN;
+    const int split = decode_resolve_split(B, Hkv, max_blocks_per_seq, block_size,
+                                           kv_split_tokens, num_sms_current_device());
+    const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
+    const int max_splits = (int)((max_ctx + split - 1) / split);
+    if (max_splits > 65535) return NV_EUNSUPPORTED;
+    plan->split_tokens = split;
+    plan->max_splits = max_splits;
+    plan->workspace_bytes = decode_workspace_bytes(B, Hq, max_splits);
+    return NV_OK;
+}
+
+bool device_addressable_for_tma(const void *p) { return tma_readable(p); }
+
 }  // namespace nvattn
 
 using namespace nvattn;
@@ -358,26 +393,15 @@ int nv_decode_attn_paged(const nv_bf16_t *q, int64_t q_tok_stride, const nv_bf16
                          int64_t num_blocks, float softmax_scale, int kv_split_tokens,
                          void *workspace, size_t workspace_bytes, int *err_count,
                          void *stream) {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks_per_seq <= 0 ||
-        block_size <= 0 || num_blocks <= 0 || kv_split_tokens < 0 || !(softmax_scale > 0.f) ||
-        !isfinite(softmax_scale))
-        return NV_EINVAL;
-    if (head_dim != 128 || block_size % 64 != 0 || Hq / Hkv > 16 || B > 65535 || Hkv > 65535)
-        return NV_EUNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * block_size > 0x7FFFFFFF || num_blocks > 0x7FFFFFFF)
-        return NV_EUNSUPPORTED;
-    if (B == 0) return NV_OK;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !o) return NV_EINVAL;
-    if (q_tok_stride < (int64_t)Hq * 128) return NV_EINVAL;
-    if (q_tok_stride % 8 || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-        !aligned16(o))
-        return NV_EALIGN;
-    const int split = decode_resolve_split(B, Hkv, max_blocks_per_seq, block_size,
-                                           kv_split_tokens, num_sms_current_device());
-    const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
-    const int max_splits = (int)((max_ctx + split - 1) / split);
-    if (max_splits > 65535) return NV_EUNSUPPORTED;
-    const size_t need = decode_workspace_bytes(B, Hq, max_splits);
+    DecodePlan plan;
+    const int st = decode_check_args(q, q_tok_stride, k_cache, v_cache, block_tables,
+                                     max_blocks_per_seq, context_lens, o, B, Hq, Hkv, head_dim,
+                                     block_size, num_blocks, softmax_scale, kv_split_tokens,
+                                     &plan);
+    if (st != NV_OK || B == 0) return st;
+    const int split = plan.split_tokens;
+    const int max_splits = plan.max_splits;
+    const size_t need = plan.workspace_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need)) return NV_EWORKSPACE;
     if (need > 0 && !aligned16(workspace)) return NV_EALIGN;
     if (!tma_readable(k_cache) || !tma_readable(v_cache)) return NV_EINVAL;

@@ -284,7 +284,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         }
     }
     named_barrier_consumers();
-    if (timed_out) return;
+    // A wait that gave up leaves this split's keys unread: its result is
+    // written as NaN, so neither the merge nor the caller can take it (or a
+    // stale workspace slot) for an answer, even without an error counter.
+    const bool failed = timed_out != 0;
     const int tid = threadIdx.x;                 // 0 .. 127
     for (int idx = tid; idx < G * 128; idx += kConsumerWarps * 32) {
         const int row = idx >> 7, d = idx & 127;
@@ -295,11 +298,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
             const float mw = comb_m[w * 16 + row];
-            const float f = fast_exp2(mw - M);   // 0 for a warp that saw no key
+            // A warp that saw no key (every tile of it skipped) adds nothing;
+            // testing for it keeps -inf - -inf out of the exponent when no
+            // warp of the split saw a key.
+            const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
             num += f * comb_o[(w * 16 + row) * kCombStride + d];
             den += f * comb_l[w * 16 + row];
         }
-        const float val = den > 0.f ? num / den : 0.f;   // den == 0 only if every key was skipped
+        // den == 0 only if every key of the split was skipped (bad block
+        // ids): the split then holds no key, its output is 0 and its
+        // log-sum-exp -inf, so the merge gives it weight 0.
+        float val = den > 0.f ? num / den : 0.f;
+        float lse = den > 0.f ? M + log2f(den) : -INFINITY;
+        if (failed) val = lse = __int_as_float(0x7fc00000);
         const int64_t head = head0 + row;
         if (n_splits == 1) {
             __nv_bfloat16 hv = __float2bfloat16_rn(val);
@@ -307,7 +318,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         } else {
             const int64_t slot = head * p.max_splits + split;
             p.ws_o[slot * 128 + d] = val;
-            if (d == 0) p.ws_lse[slot] = M + log2f(den);
+            if (d == 0) p.ws_lse[slot] = lse;
         }
     }
 }
@@ -316,6 +327,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const DecodeParams p) {
     pdl_wait_release();
+    // After a pipeline failure (this call's or an earlier one's, bit 30 of
+    // err_count) some splits wrote nothing: their workspace slots may hold an
+    // earlier call's partials.  Merge nothing and leave o as it is, as the
+    // split kernel does for the sequences it did not process.
+    if (pipeline_failed_before(p.err_count)) return;
     const int64_t wid = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= (int64_t)p.B * p.Hq) return;
@@ -335,7 +351,8 @@ decode_merge_kernel(const DecodeParams p) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float den = 0.f;
     for (int s = 0; s < n_splits; ++s) {
-        const float f = fast_exp2(lse[s] - M);
+        // A split whose keys were all skipped has lse = -inf and weight 0.
+        const float f = lse[s] == -INFINITY ? 0.f : fast_exp2(lse[s] - M);
         const float4 v = *reinterpret_cast<const float4 *>(p.ws_o + (wid * p.max_splits + s) * 128 + 4 * lane);
         acc[0] = fmaf(f, v.x, acc[0]);
         acc[1] = fmaf(f, v.y, acc[1]);

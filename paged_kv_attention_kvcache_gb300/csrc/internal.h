@@ -102,6 +102,25 @@ size_t decode_workspace_bytes(int B, int Hq, int max_splits);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, cudaStream_t s);
 
+// The host-side argument checks of nv_decode_attn_paged (everything but the
+// workspace and the memory kind of the caches) and its split plan.  Returns
+// NV_OK (plan filled; all zero when B == 0) or the NV_E* code the entry point
+// returns for these arguments.
+struct DecodePlan {
+    int split_tokens;          // keys per split
+    int max_splits;            // splits of the longest context the table allows
+    size_t workspace_bytes;    // workspace the call needs (0: none)
+};
+int decode_check_args(const void *q, int64_t q_tok_stride, const void *k_cache,
+                      const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, const void *o, int B, int Hq, int Hkv,
+                      int head_dim, int block_size, int64_t num_blocks, float softmax_scale,
+                      int kv_split_tokens, DecodePlan *plan);
+
+// True for device or managed memory (what the tensor-memory accelerator can
+// read); false for host memory or a pointer the runtime does not know.
+bool device_addressable_for_tma(const void *p);
+
 // ----------------------------------------------------------------- prefill
 struct PrefillParams {
     const int32_t *cu_seqlens_q;

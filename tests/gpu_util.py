@@ -39,15 +39,62 @@ def err_counter() -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device="cuda")
 
 
+# Every check_close result of the session, in order: (what, stats).  The
+# conftest writes them out when NV_PARITY_LOG names a file.
+PARITY_LOG = []
+
+
 def check_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str,
                 max_tol: float = MAX_TOL, mean_tol: float = MEAN_TOL) -> dict:
+    """Gate on e = |g - r| / max(1, |r|) (max and mean), and report beside it
+    the plain absolute error |g - r| (max and mean), the stated metric."""
     g = wl.bf16_bits_to_f32(gpu_bits).astype(np.float64).reshape(ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
     absdiff = np.abs(g - ref)
     e = absdiff / np.maximum(1.0, np.abs(ref))
-    stats = dict(max_err=float(e.max()) if e.size else 0.0,
-                 mean_err=float(e.mean()) if e.size else 0.0,
-                 max_abs=float(absdiff.max()) if e.size else 0.0)
+    n = int(e.size)
+    stats = dict(n=n,
+                 max_err=float(e.max()) if n else 0.0,
+                 mean_err=float(e.mean()) if n else 0.0,
+                 max_abs=float(absdiff.max()) if n else 0.0,
+                 mean_abs=float(absdiff.mean()) if n else 0.0,
+                 max_ref=float(np.abs(ref).max()) if n else 0.0)
+    PARITY_LOG.append((what, stats))
+    print(f"[parity] {what}: n={n} max|err|={stats['max_abs']:.3e} "
+          f"mean|err|={stats['mean_abs']:.3e} max e={stats['max_err']:.3e} "
+          f"mean e={stats['mean_err']:.3e} max|ref|={stats['max_ref']:.2f}")
+    assert stats["max_err"] <= max_tol, f"{what}: max err {stats}"
+    assert stats["mean_err"] <= mean_tol, f"{what}: mean err {stats}"
+    return stats
+
+
+def check_close_rows(gpu_bits: np.ndarray, ref_rows, n_rows: int, what: str, chunk: int = 2048,
+                     max_tol: float = MAX_TOL, mean_tol: float = MEAN_TOL) -> dict:
+    """check_close over every row of a large output, computed in row chunks
+    to bound host memory: ref_rows(lo, hi) returns the oracle's rows
+    [lo, hi).  The statistics are those of the whole output."""
+    n = 0
+    acc = dict(max_err=0.0, sum_err=0.0, max_abs=0.0, sum_abs=0.0, max_ref=0.0)
+    for lo in range(0, n_rows, chunk):
+        hi = min(n_rows, lo + chunk)
+        ref = ref_rows(lo, hi)
+        g = wl.bf16_bits_to_f32(gpu_bits[lo:hi]).astype(np.float64).reshape(ref.shape)
+        assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output in rows {lo}..{hi}"
+        absdiff = np.abs(g - ref)
+        e = absdiff / np.maximum(1.0, np.abs(ref))
+        n += e.size
+        acc["max_err"] = max(acc["max_err"], float(e.max()))
+        acc["sum_err"] += float(e.sum())
+        acc["max_abs"] = max(acc["max_abs"], float(absdiff.max()))
+        acc["sum_abs"] += float(absdiff.sum())
+        acc["max_ref"] = max(acc["max_ref"], float(np.abs(ref).max()))
+    stats = dict(n=n, max_err=acc["max_err"], mean_err=acc["sum_err"] / max(1, n),
+                 max_abs=acc["max_abs"], mean_abs=acc["sum_abs"] / max(1, n),
+                 max_ref=acc["max_ref"])
+    PARITY_LOG.append((what, stats))
+    print(f"[parity] {what}: n={n} max|err|={stats['max_abs']:.3e} "
+          f"mean|err|={stats['mean_abs']:.3e} max e={stats['max_err']:.3e} "
+          f"mean e={stats['mean_err']:.3e} max|ref|={stats['max_ref']:.2f}")
     assert stats["max_err"] <= max_tol, f"{what}: max err {stats}"
     assert stats["mean_err"] <= mean_tol, f"{what}: mean err {stats}"
     return stats

@@ -114,46 +114,154 @@ def test_decode_nan_in_unused_cache_rows_does_not_leak():
     check_close(got, oracle.paged_decode(q, k, v, bt, ctx, SCALE), "decode with NaN tail")
 
 
-def test_decode_bad_block_id_is_counted_not_faulted():
-    ctx = [300, 40]
+def _drop_blocks(bt_row, L, bad, bs=256):
+    """The block table and context length of the same sequence with the
+    blocks at logical indices `bad` removed: what a decode that skips those
+    keys attends over.  Only whole blocks, or the last (partial) one, are
+    removed, so the remaining keys stay in logical order."""
+    n = -(-int(L) // bs)
+    keep = [i for i in range(n) if i not in bad]
+    gone = sum(min(bs, int(L) - i * bs) for i in bad)
+    row = np.full(bt_row.shape, -1, np.int32)
+    row[:len(keep)] = bt_row[keep]
+    return row, int(L) - gone
+
+
+@pytest.mark.parametrize("split", [0, 64, 192, 256, 512])
+def test_decode_bad_block_id_is_counted_not_faulted(split):
+    # Keys of a block id outside the pool are skipped ("nano-vllm code
+    # walkthrough", Decode Stage gathers key j from block_tables[b][j / 256]);
+    # the output is attention over the keys that remain.  Cases: the last
+    # (partial) block bad, the first block bad, a middle block bad, every
+    # block bad (zeros), and an untouched sequence.  With 64- and 256-key
+    # splits a bad block fills whole splits; with 192 and 512 part of one.
+    ctx = [300, 40, 1000, 700, 200, 900]
+    bad = {0: [1], 2: [0], 3: [1], 4: [0], 5: [2]}
     q, k, v, bt, ctx = random_case(304, len(ctx), 8, 2, ctx)
     bt = bt.copy()
-    bt[0, 1] = 10_000                       # beyond the pool: keys 256..299 skipped
-    got, err = run_decode(q, k, v, bt, ctx)
-    assert err >= 1
-    # sequence 1 is unaffected
-    ref = oracle.paged_decode(q[1:], k, v, bt[1:], ctx[1:], SCALE)
-    check_close(got[1:], ref, "decode unaffected sequence")
+    for b, blocks in bad.items():
+        for i in blocks:
+            bt[b, i] = 10_000 if b % 2 == 0 else -7        # past the pool / negative
+    got, err = run_decode(q, k, v, bt, ctx, split=split)
+    assert err >= len(bad)
+    assert err & (1 << 30) == 0
+    assert np.all(np.isfinite(wl.bf16_bits_to_f32(got))), "non-finite decode output"
+    assert np.all(got[4] == 0), "a sequence with every key skipped returns zeros"
+    bt_ref = bt.copy()
+    ctx_ref = ctx.copy()
+    for b, blocks in bad.items():
+        bt_ref[b], ctx_ref[b] = _drop_blocks(bt[b], ctx[b], blocks)
+    ref = oracle.paged_decode(q, k, v, bt_ref, ctx_ref, SCALE)
+    check_close(got, ref, f"decode with bad block ids, split={split}")
 
 
-def _full_config(step: wl.DecodeStep, n_pairs, seed, split=0):
+def _planted_case(step: wl.DecodeStep, seed: int):
+    """Exact block-table indexing case on a workload's own block tables and
+    context lengths.  Query head h of sequence b is a vector u of +-1, and one
+    logical key j(b, h) of its kv head holds 32 u: its score (32 * 128 *
+    scale = 362) exceeds every other key's by more than 126 binary orders of
+    magnitude, so its softmax weight is 1 and every other weight is 0 in
+    fp32.  Every V row carries its own logical position, sequence and kv head
+    in its first five elements (integers below 256, exact in bf16).  The
+    output of (b, h) must then be V at j(b, h), bit for bit: a wrong block,
+    offset, tile or split finds another key or another V row."""
+    s = step.shape
+    B = step.context_lens.size
+    G = s.hq // s.hkv
+    bs = wl.BLOCK_SIZE
+    g = np.random.default_rng(seed)
+    ctx = step.context_lens.astype(np.int64)
+    bt = step.block_tables
+    u = g.choice(np.array([-1.0, 1.0], np.float32), size=(B, s.hq, 128))
+    q_bits = wl.f32_to_bf16_bits(u)
+    # Planted positions: distinct within each (sequence, kv head); tile,
+    # block and split edges first, then random.
+    pos = np.empty((B, s.hq), np.int64)
+    assert int(ctx.min()) >= G, "one distinct planted key per query head of a group"
+    for b in range(B):
+        L = int(ctx[b])
+        edges = [p for p in (0, L - 1, 63, 64, 255, 256, 1535, 1536, 2047, 2048, 4095, 4096,
+                             L // 2) if 0 <= p < L]
+        for kvh in range(s.hkv):
+            take = []
+            start = (b + kvh) % len(edges)
+            for i in range(len(edges)):
+                p = edges[(start + i) % len(edges)]
+                if p not in take and len(take) < G // 2:
+                    take.append(p)
+            while len(take) < G:
+                p = int(g.integers(0, L))
+                if p not in take:
+                    take.append(p)
+            pos[b, kvh * G:(kvh + 1) * G] = take
+    k = step.pool.k.copy()
+    v = step.pool.v.copy()
+    heads = np.arange(s.hq)
+    for b in range(B):
+        blk = bt[b, pos[b] // bs]
+        off = pos[b] % bs
+        k[blk, off, heads // G] = wl.f32_to_bf16_bits(32.0 * u[b])
+    # V rows: (j & 255, j >> 8, b & 255, kv head, b >> 8) in elements 0..4.
+    seq_of = np.full(step.pool.num_blocks, -1, np.int64)
+    base = np.zeros(step.pool.num_blocks, np.int64)
+    for b in range(B):
+        n = -(-int(ctx[b]) // bs)
+        seq_of[bt[b, :n]] = b
+        base[bt[b, :n]] = np.arange(n) * bs
+    used = np.nonzero(seq_of >= 0)[0]
+    j = base[used][:, None] + np.arange(bs)[None, :]
+    sq = seq_of[used][:, None] + 0 * j
+    for kvh in range(s.hkv):
+        code = np.stack([j & 255, j >> 8, sq & 255, np.full_like(j, kvh), sq >> 8], axis=-1)
+        v[used[:, None], np.arange(bs)[None, :], kvh, :5] = wl.f32_to_bf16_bits(
+            code.astype(np.float32))
+    want = np.empty((B, s.hq, 128), np.uint16)
+    for b in range(B):
+        blk = bt[b, pos[b] // bs]
+        want[b] = v[blk, pos[b] % bs, heads // G]
+    return q_bits, k, v, want
+
+
+@pytest.mark.parametrize("cfg,splits", [("config3", (0, 64, 192)), ("config5", (0, 256, 1000))])
+def test_decode_block_table_indexing_exact(cfg, splits):
+    step = getattr(wl, cfg)()
+    q_bits, k, v, want = _planted_case(step, 4400 + len(cfg))
+    kc, vc = dev(k), dev(v)
+    del k, v
+    for split in splits:
+        got, err = run_decode(q_bits, kc, vc, step.block_tables, step.context_lens, split=split)
+        assert err == 0
+        bad = np.argwhere(np.any(got != want, axis=-1))
+        assert bad.size == 0, (f"{step.name} split={split}: {len(bad)} (seq, head) outputs are "
+                               f"not the planted key's V row; first {bad[:5].tolist()}")
+
+
+def _full_config(step: wl.DecodeStep, split=0):
+    """Every (sequence, head) of a configured decode workload against the
+    oracle."""
     s = step.shape
     B = step.context_lens.size
     q_bits = step.qkv[:, :s.q_size].reshape(B, s.hq, 128)
     kc, vc = dev(step.pool.k), dev(step.pool.v)
     got, err = run_decode(q_bits, kc, vc, step.block_tables, step.context_lens, split=split)
     assert err == 0
-    g = np.random.default_rng(seed)
-    pairs = np.stack([g.integers(0, B, n_pairs), g.integers(0, s.hq, n_pairs)], axis=1)
+    del kc, vc
     ref = oracle.paged_decode(q_bits, step.pool.k, step.pool.v, step.block_tables,
-                              step.context_lens, SCALE, pairs=pairs)
-    return check_close(got[pairs[:, 0], pairs[:, 1]], ref, step.name)
+                              step.context_lens, SCALE)
+    return check_close(got, ref, f"{step.name} decode split={split or 'auto'}")
 
 
 def test_decode_qwen3_06b_batch64_full_size():
-    step = wl.config2()
-    _full_config(step, 1024, 402)
+    _full_config(wl.config2())
 
 
 def test_decode_qwen3_8b_batch256_full_size():
-    step = wl.config3()
-    _full_config(step, 256, 403)
+    _full_config(wl.config3())
 
 
 @pytest.mark.parametrize("split", [0, 256])
 def test_decode_long_context_split_kv_full_size(split):
-    step = wl.config5()
-    _full_config(step, 96, 405, split=split)
+    _full_config(wl.config5(), split=split)
 
 
 def test_decode_longest_context():

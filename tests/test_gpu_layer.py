@@ -147,8 +147,5 @@ def test_qwen3_8b_decode_step_full_size():
     got_v = host(vc.view(-1, D)[idx])
     check_cache_rows(got_k, ref_k.reshape(-1, D)[slots], "8b new k rows")
     assert np.array_equal(got_v, ref_v.reshape(-1, D)[slots])
-    g = np.random.default_rng(31)
-    pairs = np.stack([g.integers(0, B, 192), g.integers(0, s.hq, 192)], axis=1)
-    o_ref = oracle.paged_decode(qb, ref_k, ref_v, step.block_tables, step.context_lens, SCALE,
-                                pairs=pairs)
-    check_close(host(o)[pairs[:, 0], pairs[:, 1]], o_ref, "8b decode")
+    o_ref = oracle.paged_decode(qb, ref_k, ref_v, step.block_tables, step.context_lens, SCALE)
+    check_close(host(o), o_ref, "8b decode layer (B=256, every head)")

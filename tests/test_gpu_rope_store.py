@@ -111,7 +111,6 @@ def test_fused_rope_store_small_ragged_with_padding(write_k):
 def test_fused_rope_store_qwen3_8b_prefill_batch_full_size():
     pre = wl.config4()
     s = pre.shape
-    g = np.random.default_rng(610)
     nb = pre.num_blocks
     kc0 = np.zeros((nb, wl.BLOCK_SIZE, s.hkv, 128), np.uint16)
     vc0 = np.zeros_like(kc0)
@@ -120,9 +119,8 @@ def test_fused_rope_store_qwen3_8b_prefill_batch_full_size():
     assert err == 0
     q_rot, k_rot, ref_kc, ref_vc = _oracle(*args, s)
     T, Q, D = pre.qkv.shape[0], s.q_size, s.kv_size
-    rows = g.integers(0, T, 4096)
-    check_close(got_qkv[rows, :Q], q_rot.reshape(T, Q)[rows], "8b fused q")
-    check_close(got_qkv[rows, Q:Q + D], k_rot.reshape(T, D)[rows], "8b fused k")
+    check_close(got_qkv[:, :Q], q_rot.reshape(T, Q), "8b fused q (every row)")
+    check_close(got_qkv[:, Q:Q + D], k_rot.reshape(T, D), "8b fused k (every row)")
     check_cache_rows(got_kc, ref_kc, "8b fused k cache")
     assert np.array_equal(got_vc, ref_vc)
 

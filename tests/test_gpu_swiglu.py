@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import check_close, dev, host
+from gpu_util import check_close, check_close_rows, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -59,12 +59,12 @@ def test_silu_and_mul_saturated_gates():
     check_close(_run(xb), oracle.silu_and_mul(xb), "swiglu saturated")
 
 
-def test_silu_and_mul_qwen3_8b_full_size_sampled():
-    # The MLP activation of the Qwen3-8B prefill batch: ~33k tokens x 2*12288.
+def test_silu_and_mul_qwen3_8b_full_size():
+    # The MLP activation of the Qwen3-8B prefill batch: ~33k tokens x 2*12288,
+    # every output element compared (the oracle runs in row chunks).
     pre = wl.config4()
     T, I = pre.qkv.shape[0], 12288
     x = wl.normal_bf16(820, "sw.8b", (T, 2 * I))
     got = _run(x)
-    g = np.random.default_rng(821)
-    rows = np.concatenate([[0, T - 1], g.integers(0, T, 254)])
-    check_close(got[rows], oracle.silu_and_mul(x[rows]), "swiglu 8b sampled")
+    check_close_rows(got, lambda lo, hi: oracle.silu_and_mul(x[lo:hi]), T,
+                     "swiglu 8b (33k tokens x 12288)")

@@ -14,11 +14,14 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from gpu_util import check_close, dev, dev_i32, host
 
 pytestmark = pytest.mark.gpu
 
+NV_EINVAL = -1
+NV_EUNSUPPORTED = -2
 NV_EWORKSPACE = -4
 SCRATCH_BYTES = 16 << 20
 SCALE = 128 ** -0.5
@@ -42,7 +45,7 @@ def _inputs(seed, B, Hq, Hkv, ctx):
     v = wl.f32_to_bf16_bits(g.standard_normal((nb, 256, Hkv, 128)).astype(np.float32))
     q = wl.f32_to_bf16_bits(g.standard_normal((B, Hq, 128)).astype(np.float32))
     return dict(q=dev(q), k=dev(k), v=dev(v), bt=dev_i32(bt), ctx=dev_i32(ctx), B=B, Hq=Hq,
-                Hkv=Hkv, mb=bt.shape[1], nb=nb)
+                Hkv=Hkv, mb=bt.shape[1], nb=nb, host=(q, k, v, bt, ctx))
 
 
 def _both(lib, a, split):
@@ -70,21 +73,38 @@ def _both(lib, a, split):
 
 def test_no_alloc_decode_matches_workspace_decode_two_calls_in_a_row(lib):
     # Two different problems back to back: the second call finds the first
-    # call's partial results still in the shared scratch array.
+    # call's partial results still in the shared scratch array.  Both calls
+    # run the same kernels with the same split as the workspace path, so the
+    # outputs must be the same bits; each is also checked against the oracle.
     first = _inputs(901, 16, 32, 8, [4096, 300, 2500, 1024, 77, 3000, 4095, 1, 520, 2049,
                                      256, 257, 3500, 900, 4000, 128])
     second = _inputs(902, 8, 16, 8, [5000, 12, 640, 4097, 2300, 1500, 33, 999])
     for a, split in ((first, 256), (second, 512)):
         ref_bits, new_bits = _both(lib, a, split)
-        ref = wl.bf16_bits_to_f32(ref_bits).astype(np.float64)
-        check_close(new_bits, ref, f"no-alloc decode split={split}")
+        assert np.array_equal(new_bits, ref_bits), f"split={split}: outputs differ"
+        q, k, v, bt, ctx = a["host"]
+        check_close(new_bits, oracle.paged_decode(q, k, v, bt, ctx, SCALE),
+                    f"no-alloc decode split={split}")
 
 
 def test_no_alloc_decode_rejects_sizes_beyond_its_scratch(lib):
+    # Device buffers of a few bytes stand in for the tensors: a call too large
+    # for the scratch array is rejected on the host before anything launches.
     B, Hq, Hkv, mb = 256, 32, 8, 160          # 40960-token contexts, 256-key splits
     need = lib.nv_decode_attn_workspace_size(B, Hq, Hkv, 128, mb, 256, 256)
     assert need > SCRATCH_BYTES
-    fake = 0x10000                             # never dereferenced: rejected on the host
-    rc = lib.nv_decode_attn_paged_noalloc(fake, Hq * 128, fake, fake, fake, mb, fake, fake, B, Hq,
-                                          Hkv, 128, 256, 1000, SCALE, 256, None, None)
+    buf = torch.zeros(64, dtype=torch.int32, device="cuda")
+    p = buf.data_ptr()
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = lib.nv_decode_attn_paged_noalloc(p, Hq * 128, p, p, p, mb, p, p, B, Hq, Hkv, 128, 256,
+                                          1000, SCALE, 256, None, stream)
     assert rc == NV_EWORKSPACE
+    # Arguments the regular entry point rejects get its code, not
+    # NV_EWORKSPACE, even at sizes beyond the scratch array.
+    for hq, hkv, bs, want in ((30, 8, 256, NV_EINVAL), (32, 8, 96, NV_EUNSUPPORTED)):
+        rc_new = lib.nv_decode_attn_paged_noalloc(p, hq * 128, p, p, p, mb, p, p, B, hq, hkv,
+                                                  128, bs, 1000, SCALE, 256, None, stream)
+        rc_ref = lib.nv_decode_attn_paged(p, hq * 128, p, p, p, mb, p, p, B, hq, hkv, 128, bs,
+                                          1000, SCALE, 256, None, 0, None, stream)
+        assert rc_new == rc_ref == want
+    torch.cuda.synchronize()
