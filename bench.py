@@ -15,7 +15,9 @@ Reported (one JSON line on rank 0):
   e2e        the decode step through the C-ABI with pinned host inputs copied
              in and outputs copied back inside the timed region.
   cpu_baseline  the fp64 oracle on a bounded sample of the decode step.
-L2 is flushed (a 256 MB write) between timed steps, outside the events.
+L2 is flushed between timed steps, outside the events: 256 MB are written, then a
+different 256 MB buffer is read, so the timed kernels find neither their inputs
+nor dirty lines (whose write-back they would pay for) in L2.
 
 --impl reference times the oracle alone (the CPU reference arm).
 --gpus N under torchrun runs N independent replicas (the path needs no
@@ -38,9 +40,10 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 METRIC = "paged-attn decode HBM GB/s (% peak); prefill attn TFLOP/s, Qwen3-8B shape"
-WORKLOAD = ("qwen3-8b attention sublayer: decode step B=256 ctx~U[1024,8192] "
-            "(add-RMSNorm, QK-Norm+RoPE, store_kvcache, paged decode) + varlen "
-            "causal prefill 16 seqs U[128,4096]")
+WORKLOAD = ("qwen3-8b attention sublayer step: decode layer B=256 ctx~U[1024,8192] "
+            "(add-RMSNorm, QK-Norm+RoPE, store_kvcache, paged decode) + prefill layer "
+            "16 seqs U[128,4096] (add-RMSNorm, QK-Norm+RoPE, store_kvcache, varlen causal "
+            "prefill)")
 SEQ_LEN = "ctx U[1024,8192]; prefill U[128,4096]"
 SCALE = 128 ** -0.5
 
@@ -120,6 +123,22 @@ def measured_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+class L2Flush:
+    """Clears L2 between timed reps: writes a 256 MB buffer (evicting every
+    input), then reads a second one, so that L2 is left holding clean lines
+    only and the next timed kernel pays no write-back of the flush's data."""
+
+    def __init__(self, dev_t, mb: int = 256):
+        import torch
+        n = mb * 1024 * 1024 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev_t)
+        self.r = torch.zeros(n, dtype=torch.float32, device=dev_t)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 # ------------------------------------------------------- algorithmic bytes
 def decode_step_bytes(step: wl.DecodeStep) -> dict:
     s = step.shape
@@ -142,8 +161,9 @@ def prefill_flops(lengths) -> float:
 
 # ------------------------------------------------------------- clock probe
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms in a reader thread; `window()` keeps
-    the samples taken between mark_start() and mark_end()."""
+    """nvidia-smi sampled every 20 ms in a reader thread; `window()` keeps
+    the samples taken between mark_start() and mark_end(), `between(t0, t1)`
+    those of any other interval."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -157,7 +177,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             return
@@ -177,19 +197,19 @@ class ClockSampler:
     def mark_end(self):
         self.t1 = time.time()
 
-    def window(self):
-        if self.proc is None:
-            return None
-        time.sleep(0.25)
+    def stop(self):
+        if self.proc is None or self.proc.poll() is not None:
+            return
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        inside = [l for t, l in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
-        used = inside if inside else [l for _, l in self.samples[-3:]]
+
+    def summarize(self, lines):
         sm, smax, reasons = [], None, set()
-        for line in used:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -204,7 +224,20 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm), "in_window": bool(inside)}
+                "samples": len(sm)}
+
+    def between(self, t0, t1):
+        return self.summarize([l for t, l in self.samples if t0 <= t <= t1])
+
+    def window(self):
+        if self.proc is None:
+            return None
+        inside = [l for t, l in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
+        used = inside if inside else [l for _, l in self.samples[-3:]]
+        out = self.summarize(used)
+        if out is not None:
+            out["in_window"] = bool(inside)
+        return out
 
 
 # ---------------------------------------------------------------- our arm
@@ -299,7 +332,7 @@ def run_ours(args, rank, world, local_rank):
             ev[1].record()
 
     launches_per_step = (3 + decode_kernels) + 4
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev_t)
+    flush = L2Flush(dev_t)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -319,7 +352,7 @@ def run_ours(args, rank, world, local_rank):
     clocks.mark_start()
     t_wall = time.time()
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         e = [ev() for _ in range(6)]
         e[0].record()
         decode_layer(ev=(e[1], e[2]))
@@ -332,6 +365,32 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk = clocks.window()
+
+    # ---- clock block: the same step repeated for at least 1.2 s (L2 not
+    # flushed), so that clock samples taken every 20 ms cover the work they
+    # are quoted with: time x median SM clock gives cycles per step.
+    mean_step_ms = statistics.mean(e[0].elapsed_time(e[3]) + e[3].elapsed_time(e[5])
+                                   for e in records)
+    n_blk = max(50, int(1.2e3 / max(0.1, mean_step_ms)))
+    torch.cuda.synchronize()
+    eb0, eb1 = ev(), ev()
+    tb0 = time.time()
+    eb0.record()
+    for _ in range(n_blk):
+        decode_layer()
+        prefill_layer()
+    eb1.record()
+    torch.cuda.synchronize()
+    tb1 = time.time()
+    blk_ms = eb0.elapsed_time(eb1) / n_blk
+    bclk = clocks.between(tb0, tb1)
+    clocks.stop()
+    clock_block = {"steps": n_blk, "seconds": round(tb1 - tb0, 3), "ms_per_step": blk_ms,
+                   "l2": "not flushed"}
+    if bclk:
+        clock_block.update(sm_mhz_median=bclk["sm_mhz"], sm_max_mhz=bclk["sm_max_mhz"],
+                           reasons=bclk["reasons"], samples=bclk["samples"],
+                           kcycles_per_step=blk_ms * bclk["sm_mhz"])
     dec_ms = [e[0].elapsed_time(e[3]) for e in records]
     attn_ms = [e[1].elapsed_time(e[2]) for e in records]
     pre_ms = [e[3].elapsed_time(e[5]) for e in records]
@@ -385,7 +444,7 @@ def run_ours(args, rank, world, local_rank):
     q2, k2, v2 = decode_views(dv["qkv"])
     e2e_ms = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         e0, e1 = ev(), ev()
         e0.record()
         nv.nv_add_rmsnorm(host_x, host_r, d_g, host_y, host_rout, eps=wl.RMS_EPS)
@@ -402,7 +461,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_val = job_throughput(nbytes["total"], world, e2e_s) / 1e9
 
     graph_info = graph_decode_overhead(dev_t)
-    decode_sets = decode_attention_configs(dev_t)
+    decode_sets_out = decode_sets(dev_t, measured_peaks()[0])
     prefix_prefill = prefill_prefix_config(dev_t)
 
     # ---- QK-Norm + RoPE + store on the prefill batch: two kernels vs one pass
@@ -434,6 +493,9 @@ def run_ours(args, rank, world, local_rank):
                   "pair_bytes": pair_bytes, "fused_bytes": fused_bytes,
                   "fused_gbs": fused_bytes / (fused_us * 1e-6) / 1e9,
                   "pair_gbs": pair_bytes / (pair_us * 1e-6) / 1e9}
+    hbm_peak = measured_peaks()[0]
+    rope_store["fused_frac"] = rope_store["fused_gbs"] / hbm_peak
+    rope_store["pair_frac"] = rope_store["pair_gbs"] / hbm_peak
     assert int(err.item()) == 0, f"device error count {int(err.item())}"
 
     # ---- the MLP's SiluAndMul on the prefill batch (Qwen3-8B intermediate 12288)
@@ -444,66 +506,121 @@ def run_ours(args, rank, world, local_rank):
     swiglu_bytes = T * 3 * inter * 2
     swiglu = {"tokens": T, "intermediate": inter, "us": swiglu_us, "bytes": swiglu_bytes,
               "gbs": swiglu_bytes / (swiglu_us * 1e-6) / 1e9}
+    swiglu["frac"] = swiglu["gbs"] / hbm_peak
     del gate_up, act
 
     return dict(
-        graph=graph_info, rope_store=rope_store, swiglu=swiglu, decode_sets=decode_sets,
+        graph=graph_info, rope_store=rope_store, swiglu=swiglu, decode_sets=decode_sets_out,
         prefix_prefill=prefix_prefill,
         value=value, ms_per_step=tot_ms / args.steps, dec_ms=statistics.mean(dec_ms),
         pre_ms=statistics.mean(pre_ms), attn_ms=statistics.mean(attn_ms),
         attn_gbs=attn_gbs, ptflops=ptflops, pattn_ms=pattn_sum / args.steps, clocks=clk,
+        clock_block=clock_block,
         hbm=hbm, bf16=bf16, bf16_sus=bf16_sus, peak_src=peak_src, nbytes=nbytes,
         launches=launches_per_step * args.steps, e2e=e2e_val, h2d=h2d, d2h=d2h, wall=wall,
         gen_s=gen_s, step=step, pre=pre, ws_bytes=ws_bytes, T=T)
 
 
-# ------------------------------------ decode attention on the other decode sets
-def decode_attention_configs(dev_t, reps: int = 20):
-    """Paged decode attention alone on the two other decode workloads: Qwen3-0.6B
-    heads, B=64, ctx U[512, 4096] (0.6 GB of K/V), and Qwen3-8B heads, B=32, ctx
-    log-uniform in [4096, 40960] with 1% outlier K rows (2.1 GB), with the
-    automatic split and a forced 1024-key split.  L2 flushed before each rep;
-    median of `reps` event-timed launches."""
+# ------------------------------------------------------ the other decode sets
+def store_decode_bytes(step: wl.DecodeStep) -> dict:
+    """Algorithmic bytes of a decode step without the norms: store_kvcache of
+    the new token's K/V (read k, v; write both cache rows; slot) and paged
+    decode attention (K/V read once per kv head, q, o, block table, context)."""
+    s = step.shape
+    B = step.context_lens.size
+    Q, D = s.q_size, s.kv_size
+    ctx = step.context_lens.astype(np.int64)
+    blocks = np.ceil(ctx / wl.BLOCK_SIZE).astype(np.int64)
+    store = B * D * 2 * 4 + B * 4
+    attn = int(ctx.sum()) * D * 2 * 2 + B * Q * 2 * 2 + int(blocks.sum()) * 4 + B * 4
+    return dict(store=store, attn=attn, total=store + attn)
+
+
+def decode_sets(dev_t, hbm_peak: float, reps: int = 20):
+    """The two other decode workloads, each timed (L2 flushed before each rep,
+    median of `reps` event-timed reps):
+      Qwen3-0.6B heads, B=64, ctx U[512, 4096]: the whole step as the pages run
+        it -- store_kvcache of each sequence's new token, then paged decode --
+        and the attention call alone;
+      Qwen3-8B heads, B=32, ctx log-U[4096, 40960], 1% outlier K rows: paged
+        decode with the automatic split and with forced 1024-key splits."""
     import torch
     import paged_kv_attention_kvcache_gb300 as nv
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev_t)
+    flush = L2Flush(dev_t)
 
     def dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
             torch.bfloat16).to(dev_t)
 
+    def timed(fn):
+        times = []
+        for i in range(reps + 3):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) / 1e3)
+        return statistics.median(times)
+
+    def entry(nbytes, t, B, what):
+        gbs = nbytes / t / 1e9
+        return {"what": what, "bytes": nbytes, "ms": t * 1e3, "gbs": gbs,
+                "frac": gbs / hbm_peak, "tokens_per_s": B / t}
+
     out = {}
-    for name, step, splits in (("b64_ctx512_4096_qwen3_06b", wl.config2(), (0,)),
-                               ("b32_ctx4096_40960_qwen3_8b", wl.config5(), (0, 1024))):
-        s = step.shape
-        B = step.context_lens.size
-        q = dev(step.qkv[:, :s.q_size]).view(B, s.hq, 128)
-        kc, vc = dev(step.pool.k), dev(step.pool.v)
-        bt = torch.from_numpy(step.block_tables).to(dev_t)
-        cl = torch.from_numpy(step.context_lens).to(dev_t)
-        o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
-        nbytes = decode_step_bytes(step)["attn"]
-        for split in splits:
-            wsb = nv.nv_decode_attn_workspace_size(B, s.hq, s.hkv, 128, bt.shape[1],
-                                                   wl.BLOCK_SIZE, split)
-            ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
-            times = []
-            for i in range(reps + 3):
-                flush.zero_()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-                nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws,
-                                        kv_split_tokens=split)
-                e1.record()
-                torch.cuda.synchronize()
-                if i >= 3:
-                    times.append(e0.elapsed_time(e1) / 1e3)
-            t = statistics.median(times)
-            out[f"{name}_split{split or 'auto'}"] = {"kv_bytes": nbytes, "ms": t * 1e3,
-                                                      "gbs": nbytes / t / 1e9}
-        del kc, vc
-    del flush
+    # ---- Qwen3-0.6B heads, B = 64: store then decode
+    step = wl.config2()
+    s = step.shape
+    B, Q, D = step.context_lens.size, s.q_size, s.kv_size
+    qkv = dev(step.qkv)
+    q = qkv[:, :Q].view(B, s.hq, 128)
+    k = qkv[:, Q:Q + D].view(B, s.hkv, 128)
+    v = qkv[:, Q + D:].view(B, s.hkv, 128)
+    kc, vc = dev(step.pool.k), dev(step.pool.v)
+    bt = torch.from_numpy(step.block_tables).to(dev_t)
+    cl = torch.from_numpy(step.context_lens).to(dev_t)
+    slots = torch.from_numpy(step.slot_mapping).to(dev_t)
+    o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
+    wsb = nv.nv_decode_attn_workspace_size(B, s.hq, s.hkv, 128, bt.shape[1], wl.BLOCK_SIZE, 0)
+    ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
+    nb = store_decode_bytes(step)
+
+    def attn():
+        nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws)
+
+    def full_step():
+        nv.nv_store_kvcache(k, v, kc, vc, slots)
+        attn()
+
+    out["b64_ctx512_4096_qwen3_06b_step"] = entry(
+        nb["total"], timed(full_step), B, "store_kvcache of 64 new tokens + paged decode")
+    out["b64_ctx512_4096_qwen3_06b_attn"] = entry(nb["attn"], timed(attn), B,
+                                                   "paged decode alone")
+    out["b64_ctx512_4096_qwen3_06b_attn"]["kv_bytes"] = nb["attn"]
+    del kc, vc, qkv
+    # ---- Qwen3-8B heads, B = 32, long contexts
+    step = wl.config5()
+    s = step.shape
+    B = step.context_lens.size
+    q = dev(step.qkv[:, :s.q_size]).view(B, s.hq, 128)
+    kc, vc = dev(step.pool.k), dev(step.pool.v)
+    bt = torch.from_numpy(step.block_tables).to(dev_t)
+    cl = torch.from_numpy(step.context_lens).to(dev_t)
+    o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16, device=dev_t)
+    nbytes = store_decode_bytes(step)["attn"]
+    for split in (0, 1024):
+        wsb = nv.nv_decode_attn_workspace_size(B, s.hq, s.hkv, 128, bt.shape[1],
+                                               wl.BLOCK_SIZE, split)
+        ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device=dev_t)
+        t = timed(lambda: nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws,
+                                                  kv_split_tokens=split))
+        out[f"b32_ctx4096_40960_qwen3_8b_split{split or 'auto'}"] = entry(
+            nbytes, t, B, f"paged decode, {'automatic' if not split else '1024-key'} split")
+    del kc, vc, flush
     return out
 
 
@@ -530,7 +647,7 @@ def prefill_prefix_config(dev_t, reps: int = 20):
     def dev_i32(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev_t)
 
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev_t)
+    flush = L2Flush(dev_t)
     q, kc, vc = dev(pre.q), dev(pre.pool.k), dev(pre.pool.v)
     kk, vv = wl.gather_paged(pre.pool, pre.block_tables, pre.prefix + pre.new)
     dk, dvv = dev(kk), dev(vv)
@@ -550,7 +667,7 @@ def prefill_prefix_config(dev_t, reps: int = 20):
     for name, fn in calls.items():
         times = []
         for i in range(reps + 3):
-            flush.zero_()
+            flush()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -560,7 +677,8 @@ def prefill_prefix_config(dev_t, reps: int = 20):
             if i >= 3:
                 times.append(e0.elapsed_time(e1) / 1e3)
         t = statistics.median(times)
-        out[name] = {"ms": t * 1e3, "tflops": flops / t / 1e12}
+        out[name] = {"ms": t * 1e3, "tflops": flops / t / 1e12,
+                     "frac": flops / t / 1e12 / measured_peaks()[1]}
     del flush, kc, vc, dk, dvv
     return out
 
@@ -650,8 +768,8 @@ def graph_decode_overhead(dev_t, buckets=(1, 8, 64, 512), ctx_len: int = 1024, r
 # ------------------------------------------------------------ oracle side
 def oracle_decode_step(step: wl.DecodeStep):
     """The fp64 oracle on the whole decode step: add-RMSNorm, QK-Norm + RoPE
-    of q and k, and paged decode of every (sequence, head).  Returns
-    (seconds, threads)."""
+    of q and k, store_kvcache of the new rows and paged decode of every
+    (sequence, head).  Returns (seconds, threads)."""
     import oracle
     s = step.shape
     B = step.context_lens.size
@@ -660,11 +778,39 @@ def oracle_decode_step(step: wl.DecodeStep):
     oracle.add_rmsnorm(step.x, step.residual, step.gamma, wl.RMS_EPS)
     qb = step.qkv[:, :Q].reshape(B, s.hq, 128)
     kb = step.qkv[:, Q:Q + D].reshape(B, s.hkv, 128)
+    vb = step.qkv[:, Q + D:].reshape(B, s.hkv, 128)
     q_rot = oracle.round_to_bf16(oracle.qknorm_rope(qb, step.q_norm_w, step.positions))
-    oracle.qknorm_rope(kb, step.k_norm_w, step.positions)
+    k_rot = oracle.round_to_bf16(oracle.qknorm_rope(kb, step.k_norm_w, step.positions))
+    oracle.store_kvcache(k_rot, vb, step.pool.k, step.pool.v, step.slot_mapping)
     oracle.paged_decode(q_rot, step.pool.k, step.pool.v, step.block_tables, step.context_lens,
                         SCALE)
     return time.time() - t0, oracle.num_threads()
+
+
+def oracle_store_decode(step: wl.DecodeStep):
+    """The oracle on a decode step without the norms: store_kvcache of the new
+    token's K/V, then paged decode.  Returns seconds."""
+    import oracle
+    s = step.shape
+    B = step.context_lens.size
+    Q, D = s.q_size, s.kv_size
+    t0 = time.time()
+    oracle.store_kvcache(step.qkv[:, Q:Q + D].reshape(B, s.hkv, 128),
+                         step.qkv[:, Q + D:].reshape(B, s.hkv, 128), step.pool.k, step.pool.v,
+                         step.slot_mapping)
+    oracle.paged_decode(step.qkv[:, :Q].reshape(B, s.hq, 128), step.pool.k, step.pool.v,
+                        step.block_tables, step.context_lens, SCALE)
+    return time.time() - t0
+
+
+def repeat_for(fn, min_seconds: float):
+    """Call fn() (which returns its own seconds) until min_seconds have been
+    spent; returns (calls, seconds)."""
+    n, total = 0, 0.0
+    while n == 0 or total < min_seconds:
+        total += fn()
+        n += 1
+    return n, total
 
 
 def oracle_baseline(step: wl.DecodeStep, min_seconds: float = 10.0):
@@ -675,6 +821,138 @@ def oracle_baseline(step: wl.DecodeStep, min_seconds: float = 10.0):
         dt, threads = oracle_decode_step(step)
         times.append(dt)
     return nbytes * len(times) / sum(times) / 1e9, threads, len(times), sum(times)
+
+
+def visible_keys(cu_q: np.ndarray, cu_k: np.ndarray) -> np.ndarray:
+    """Keys each packed query token sees under causality aligned to the last
+    key: i + (Lk - Lq) + 1 for query i of its sequence."""
+    lq = np.diff(cu_q).astype(np.int64)
+    lk = np.diff(cu_k).astype(np.int64)
+    seq = np.repeat(np.arange(lq.size), lq)
+    i = np.arange(int(cu_q[-1]), dtype=np.int64) - cu_q[:-1].astype(np.int64)[seq]
+    return i + (lk - lq)[seq] + 1
+
+
+def oracle_attention_rate(call, vis: np.ndarray, hq: int, min_seconds: float, seed: int,
+                          chunk: int = 4096):
+    """TFLOP/s of the oracle's attention over credited row samples: chunks of
+    `chunk` random (token, head) rows, each credited with its own causal
+    pairs (4 * 128 * visible keys), until min_seconds of work.  `call(rows)`
+    runs the oracle on the rows.  Returns (tflops, rows, seconds)."""
+    g = np.random.default_rng(seed)
+    flops, total, n = 0.0, 0.0, 0
+    while n == 0 or total < min_seconds:
+        toks = g.integers(0, vis.size, chunk)
+        rows = np.stack([toks, g.integers(0, hq, chunk)], axis=1).astype(np.int64)
+        t0 = time.time()
+        call(rows)
+        total += time.time() - t0
+        flops += 4.0 * 128 * float(vis[toks].sum())
+        n += chunk
+    return flops / total / 1e12, n, total
+
+
+def oracle_figures(r: dict, min_seconds: float = 4.0) -> dict:
+    """The fp64 oracle timed on the host cores beside every throughput of the
+    bench line other than the headline decode step, in the same units.  Each
+    is a bounded sample, described in its `sample` field."""
+    import oracle
+    threads = oracle.num_threads()
+    out = {}
+    pre = r["pre"]
+    s = pre.shape
+    T, Q, D = pre.qkv.shape[0], s.q_size, s.kv_size
+    q = pre.qkv[:, :Q].reshape(T, s.hq, 128)
+    k = pre.qkv[:, Q:Q + D].reshape(T, s.hkv, 128)
+    v = pre.qkv[:, Q + D:].reshape(T, s.hkv, 128)
+    cu = pre.cu_seqlens
+    # ---- prefill attention (cfg4 batch), credited rows
+    tf, n, secs = oracle_attention_rate(
+        lambda rows: oracle.attention_varlen(q, k, v, cu, cu, SCALE, True, rows=rows),
+        visible_keys(cu, cu), s.hq, min_seconds, 7001)
+    out["prefill_attention"] = {
+        "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "sample": f"{n} random (token, head) rows of the 33k-token batch, each credited with "
+                  f"its causal pairs; {secs:.1f} s"}
+    # ---- the prefill layer's other ops on the whole batch, then tokens/s of the
+    # layer with attention at the rate just measured
+    t0 = time.time()
+    oracle.add_rmsnorm(pre.x, pre.residual, pre.gamma, wl.RMS_EPS)
+    oracle.qknorm_rope(q, pre.q_norm_w, pre.positions)
+    k_rot = oracle.round_to_bf16(oracle.qknorm_rope(k, pre.k_norm_w, pre.positions))
+    kc = np.zeros((pre.num_blocks, wl.BLOCK_SIZE, s.hkv, 128), np.uint16)
+    vc = np.zeros_like(kc)
+    oracle.store_kvcache(k_rot, v, kc, vc, pre.slot_mapping)
+    t_elem = time.time() - t0
+    t_attn = prefill_flops(pre.lengths) / (tf * 1e12)
+    out["prefill_layer_tokens_per_s"] = {
+        "value": T / (t_elem + t_attn), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "sample": f"add-RMSNorm, QK-Norm+RoPE and store_kvcache of all {T} tokens timed "
+                  f"({t_elem:.1f} s); attention at the sampled rate above"}
+    # ---- QK-Norm + RoPE + store on the prefill batch (the fused pass's bytes)
+    t0 = time.time()
+    oracle.qknorm_rope(q, pre.q_norm_w, pre.positions)
+    k_rot = oracle.round_to_bf16(oracle.qknorm_rope(k, pre.k_norm_w, pre.positions))
+    oracle.store_kvcache(k_rot, v, kc, vc, pre.slot_mapping)
+    t_rs = time.time() - t0
+    out["rope_store_prefill"] = {
+        "value": r["rope_store"]["fused_bytes"] / t_rs / 1e9, "unit": "GB/s", "cores": threads,
+        "kind": "oracle", "sample": f"QK-Norm+RoPE of q and k, store_kvcache, all {T} tokens, "
+                                    f"credited with the fused pass's bytes; {t_rs:.1f} s"}
+    del kc, vc
+    # ---- SiluAndMul, credited rows of the [T, 2 x 12288] activation
+    inter = 12288
+    xs = wl.normal_bf16(830, "bench.swiglu", (1024, 2 * inter))
+
+    def swiglu():
+        t0 = time.time()
+        oracle.silu_and_mul(xs)
+        return time.time() - t0
+
+    calls, secs = repeat_for(swiglu, min_seconds / 2)
+    out["silu_and_mul_prefill"] = {
+        "value": calls * 1024 * 3 * inter * 2 / secs / 1e9, "unit": "GB/s", "cores": threads,
+        "kind": "oracle", "sample": f"1024 rows x 12288 repeated {calls}x ({secs:.1f} s), "
+                                    f"credited with 3 x 2 bytes per element"}
+    # ---- decode sets
+    st2 = wl.config2()
+    nb2 = store_decode_bytes(st2)
+    calls, secs = repeat_for(lambda: oracle_store_decode(st2), min_seconds)
+    B2 = st2.context_lens.size
+    out["b64_ctx512_4096_qwen3_06b_step"] = {
+        "value": nb2["total"] * calls / secs / 1e9, "unit": "GB/s",
+        "tokens_per_s": B2 * calls / secs, "cores": threads, "kind": "oracle",
+        "sample": f"store_kvcache + paged decode of all 64 sequences, {calls}x ({secs:.1f} s)"}
+    del st2
+    st5 = wl.config5()
+    nb5 = store_decode_bytes(st5)["attn"]
+    B5 = st5.context_lens.size
+    qb5 = st5.qkv[:, :st5.shape.q_size].reshape(B5, st5.shape.hq, 128)
+
+    def dec5():
+        t0 = time.time()
+        oracle.paged_decode(qb5, st5.pool.k, st5.pool.v, st5.block_tables, st5.context_lens,
+                            SCALE)
+        return time.time() - t0
+
+    calls, secs = repeat_for(dec5, min_seconds)
+    out["b32_ctx4096_40960_qwen3_8b"] = {
+        "value": nb5 * calls / secs / 1e9, "unit": "GB/s", "tokens_per_s": B5 * calls / secs,
+        "cores": threads, "kind": "oracle",
+        "sample": f"paged decode of all 32 sequences (unsplit), {calls}x ({secs:.1f} s)"}
+    del st5
+    # ---- prefill over the paged cache (prefix hit), credited rows
+    px = wl.config_prefix()
+    tf, n, secs = oracle_attention_rate(
+        lambda rows: oracle.attention_paged_prefill(px.q, px.pool.k, px.pool.v, px.block_tables,
+                                                    px.cu_seqlens_q, px.cu_seqlens_k, SCALE,
+                                                    rows=rows),
+        visible_keys(px.cu_seqlens_q, px.cu_seqlens_k), px.shape.hq, min_seconds, 7002)
+    out["prefill_paged_prefix"] = {
+        "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "sample": f"{n} random (token, head) rows of the prefix-hit workload, each credited "
+                  f"with its causal pairs; {secs:.1f} s"}
+    return out
 
 
 def slice_decode_step(step: wl.DecodeStep, idx: np.ndarray) -> wl.DecodeStep:
@@ -691,37 +969,61 @@ def slice_decode_step(step: wl.DecodeStep, idx: np.ndarray) -> wl.DecodeStep:
 
 
 def run_reference(args, budget_s: float = 150.0):
-    """The CPU reference arm: the fp64 oracle, as it stands, on the same
-    decode-step workload.  One untimed pass of the whole step sizes the run:
-    if `steps` whole passes would take longer than `budget_s`, each step takes
-    a rotating slice of the sequences (a bounded sample) and is credited with
-    that slice's algorithmic bytes."""
+    """The CPU reference arm: the fp64 oracle, as it stands, on the bench's
+    workload.  Each step is the decode layer step (the line's value) and a
+    sample of the prefill layer: one chunk of 2048 random (token, head)
+    attention rows of the 33k-token batch, credited with their causal pairs.
+    One untimed pass of the whole decode step sizes the run: if `steps` whole
+    passes would take longer than `budget_s`, each step takes a rotating slice
+    of the sequences (a bounded sample) credited with that slice's bytes."""
     import oracle
     oracle.build()
     step = wl.config3()
+    pre = wl.config4()
+    s = pre.shape
+    T, Q, D = pre.qkv.shape[0], s.q_size, s.kv_size
+    pq = pre.qkv[:, :Q].reshape(T, s.hq, 128)
+    pk = pre.qkv[:, Q:Q + D].reshape(T, s.hkv, 128)
+    pv = pre.qkv[:, Q + D:].reshape(T, s.hkv, 128)
+    cu = pre.cu_seqlens
+    vis = visible_keys(cu, cu)
     B = step.context_lens.size
     t_full, threads = oracle_decode_step(step)
     per = B
     if args.steps * t_full > budget_s:
         per = max(8, min(B, int(B * budget_s / (args.steps * t_full))))
-    times, nbytes = [], 0
+    g = np.random.default_rng(7003)
+    times, ptimes, nbytes, pflops = [], [], 0, 0.0
     for k in range(args.steps):
         sub = step if per == B else slice_decode_step(step, (k * per + np.arange(per)) % B)
         dt, threads = oracle_decode_step(sub)
         times.append(dt)
         nbytes += decode_step_bytes(sub)["total"]
+        toks = g.integers(0, T, 2048)
+        rows = np.stack([toks, g.integers(0, s.hq, 2048)], axis=1).astype(np.int64)
+        t0 = time.time()
+        oracle.attention_varlen(pq, pk, pv, cu, cu, SCALE, True, rows=rows)
+        ptimes.append(time.time() - t0)
+        pflops += 4.0 * 128 * float(vis[toks].sum())
     value = nbytes / sum(times) / 1e9
-    sample = (f"qwen3-8b decode step (32 heads, ctx~U[1024,8192]): add-RMSNorm, QK-Norm+RoPE, "
-              f"paged decode; {per} of its {B} sequences per step"
-              + (" (rotating slice), credited with their own bytes" if per < B else ""))
+    ptf = pflops / sum(ptimes) / 1e12
+    sample = (f"decode layer step (32 heads, ctx~U[1024,8192]): add-RMSNorm, QK-Norm+RoPE, "
+              f"store_kvcache, paged decode; {per} of its {B} sequences per step"
+              + (" (rotating slice), credited with their own bytes" if per < B else "")
+              + "; plus 2048 random prefill attention rows per step, credited with their "
+                "causal pairs")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * (sum(times) + sum(ptimes)) / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": 256, "seq_len": SEQ_LEN,
                    "parallelism": "single", "decode_step_bytes": decode_step_bytes(step)["total"],
-                   "timed": "the decode step (the line's value) in the fp64 CPU oracle"},
+                   "timed": "the decode layer step (the line's value) and a sample of the "
+                            "prefill layer's attention, in the fp64 CPU oracle"},
+        "prefill": {"metric": "prefill attn TFLOP/s (causal pairs)", "value": ptf,
+                    "unit": "TFLOP/s"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -863,11 +1165,22 @@ def main():
     r = run_ours(args, rank, world, local_rank)
 
     cpu = None
+    ofig = {}
     if rank == 0 and not args.no_cpu_baseline:
         val, threads, reps, secs = oracle_baseline(r["step"])
         cpu = {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "tokens_per_s": r["step"].context_lens.size * reps / secs,
                "sample": f"whole decode step (256 seqs x 32 heads: add-RMSNorm, QK-Norm+RoPE, "
-                         f"paged decode) repeated {reps}x, {secs:.1f} s of CPU time"}
+                         f"store_kvcache, paged decode) repeated {reps}x, {secs:.1f} s of CPU "
+                         f"time"}
+        ofig = oracle_figures(r)
+        r["decode_sets"]["b64_ctx512_4096_qwen3_06b_step"]["oracle"] = \
+            ofig["b64_ctx512_4096_qwen3_06b_step"]
+        for key in ("b32_ctx4096_40960_qwen3_8b_splitauto", "b32_ctx4096_40960_qwen3_8b_split1024"):
+            r["decode_sets"][key]["oracle"] = ofig["b32_ctx4096_40960_qwen3_8b"]
+        r["prefix_prefill"]["oracle"] = ofig["prefill_paged_prefix"]
+        r["rope_store"]["oracle"] = ofig["rope_store_prefill"]
+        r["swiglu"]["oracle"] = ofig["silu_and_mul_prefill"]
     if rank == 0:
         nbytes = r["nbytes"]
         B_dec = r["step"].context_lens.size
@@ -884,7 +1197,7 @@ def main():
                 "global_batch": 256 * world, "seq_len": SEQ_LEN,
                 "parallelism": "replicas" if world > 1 else "single",
                 "decode_kv_bytes": nbytes["attn"], "decode_step_bytes": nbytes["total"],
-                "prefill_tokens": r["T"], "l2": "flushed (256 MB write) between steps",
+                "prefill_tokens": r["T"], "l2": "flushed between steps (256 MB written, then another 256 MB read)",
                 "decode_ms": r["dec_ms"], "prefill_ms": r["pre_ms"]},
             "roofline": {"bound": "hbm", "kernel": "nv_decode_attn_paged (split + merge)",
                          "achieved": r["attn_gbs"], "peak": r["hbm"], "unit": "GB/s",
@@ -892,6 +1205,7 @@ def main():
                          "peak_source": r["peak_src"], "launch_ms": r["attn_ms"]},
             "prefill": {"metric": "prefill attn TFLOP/s (causal pairs)", "value": r["ptflops"],
                         "unit": "TFLOP/s", "launch_ms": r["pattn_ms"],
+                        "oracle": ofig.get("prefill_attention"),
                         "roofline": {"bound": "tensor", "achieved": r["ptflops"],
                                      "peak": r["bf16"], "unit": "TFLOP/s",
                                      "frac": r["ptflops"] / r["bf16"],
@@ -904,7 +1218,11 @@ def main():
             "e2e": {"value": r["e2e"], "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]},
             "tokens_per_s": {"decode": world * B_dec / (r["dec_ms"] / 1e3),
-                             "prefill": world * r["T"] / (r["pre_ms"] / 1e3)},
+                             "prefill": world * r["T"] / (r["pre_ms"] / 1e3),
+                             "oracle_decode": cpu["tokens_per_s"] if cpu else None,
+                             "oracle_prefill": (ofig["prefill_layer_tokens_per_s"]["value"]
+                                                if ofig else None),
+                             "oracle_cores": cpu["cores"] if cpu else None},
             "nominal_frac": {"decode_attn_of_7900_GBs": r["attn_gbs"] / 7900.0,
                              "prefill_of_2250_TFLOPs": r["ptflops"] / 2250.0},
             "decode_attention_sets": r["decode_sets"],
@@ -914,6 +1232,7 @@ def main():
             "silu_and_mul_prefill": r["swiglu"],
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
+            "clock_block": r["clock_block"],
         }
         print(json.dumps(line))
     if world > 1:

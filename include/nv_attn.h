@@ -107,16 +107,19 @@ NV_API int nv_rope_cos_sin_cache(float *cos_sin, int max_position, int rotary_di
  *   out = bf16(s * rsqrt(mean(s^2) + eps) * weight)
  * residual == NULL gives the plain RMSNorm of x (first layer); residual_out
  * is then not written and may be NULL.
- *   x, residual, out, residual_out   [T, H] bf16, contiguous rows.
+ *   x, residual, out, residual_out   [T, H] bf16; row t of each starts
+ *                                    row_stride elements after row t - 1
+ *                                    (row_stride == H: contiguous rows).
  *   weight                           [H] bf16 (gamma).
  * residual_out may alias residual (in place); out may alias x.  Other
- * overlaps are undefined.  Requires H % 8 == 0, 8 <= H <= 16384, all
- * pointers 16-byte aligned.  T == 0 is a no-op.
+ * overlaps are undefined.  Requires H % 8 == 0, 8 <= H <= 16384,
+ * row_stride >= H and a multiple of 8, all pointers 16-byte aligned.
+ * T == 0 is a no-op.
  */
 NV_API int nv_add_rmsnorm(const nv_bf16_t *x, const nv_bf16_t *residual,
                    const nv_bf16_t *weight, nv_bf16_t *out,
-                   nv_bf16_t *residual_out, int64_t T, int H, float eps,
-                   void *stream);
+                   nv_bf16_t *residual_out, int64_t T, int H,
+                   int64_t row_stride, float eps, void *stream);
 
 /*
  * QK-Norm + RoPE, in place.  "3.3 Model skeleton and core operators",
@@ -258,8 +261,9 @@ NV_API int nv_silu_and_mul(const nv_bf16_t *x, int64_t x_tok_stride, nv_bf16_t *
  * plain prefill and Lk > Lq a prefill whose first Lk - Lq keys are an
  * earlier prefix.  Requires causal == 1 and Lk >= Lq for every sequence (a
  * sequence with Lk < Lq is skipped and counted in err_count).  Rows of other
- * sequences that share a 128-row tile are read but masked, so every row of
- * k and v must hold finite values.
+ * sequences that share a 128-row tile are read but masked, and V rows past a
+ * sequence's last key are zeroed in shared memory before use, so another
+ * sequence's rows may hold any bits (NaN included) without reaching o.
  * Requires head_dim == 128, token strides multiples of 8, 16-byte aligned
  * pointers, total_q, total_k < 2^31.  err_count (optional) counts skipped
  * sequences and records NV_ERR_PIPELINE_FAILURE.

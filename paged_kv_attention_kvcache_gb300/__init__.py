@@ -43,7 +43,7 @@ _SIGNATURES = {
     "nv_status_string": ([_I32], ctypes.c_char_p),
     "nv_version": ([], _I32),
     "nv_rope_cos_sin_cache": ([_P, _I32, _I32, _F64, _P], _I32),
-    "nv_add_rmsnorm": ([_P, _P, _P, _P, _P, _I64, _I32, _F32, _P], _I32),
+    "nv_add_rmsnorm": ([_P, _P, _P, _P, _P, _I64, _I32, _I64, _F32, _P], _I32),
     "nv_qknorm_rope": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _P, _I64, _I32, _I32, _I32, _F32,
                         _P, _P], _I32),
     "nv_store_kvcache": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I64, _P, _P], _I32),
@@ -130,14 +130,22 @@ def nv_rope_cos_sin_cache(cos_sin: torch.Tensor, base: float = 1e6, stream=None)
 
 def nv_add_rmsnorm(x, residual, weight, out, residual_out=None, eps: float = 1e-6,
                    stream=None) -> None:
-    """out = RMSNorm(x + residual) * weight; residual_out = x + residual."""
+    """out = RMSNorm(x + residual) * weight; residual_out = x + residual.
+
+    x, residual, out, residual_out: [T, H] views whose rows share one row
+    stride (elements) and whose elements within a row are contiguous."""
     T, H = x.shape
+    stride = x.stride(0) if T > 1 else H
     for t in (x, residual, out, residual_out):
-        if t is not None and not t.is_contiguous():
-            raise ValueError("add_rmsnorm tensors must be contiguous")
+        if t is None:
+            continue
+        if tuple(t.shape) != (T, H) or (H > 1 and t.stride(1) != 1):
+            raise ValueError("add_rmsnorm tensors must be [T, H] with contiguous rows")
+        if T > 1 and t.stride(0) != stride:
+            raise ValueError("add_rmsnorm tensors must share one row stride")
     _check("nv_add_rmsnorm", library().nv_add_rmsnorm(
-        _ptr(x), _ptr(residual), _ptr(weight), _ptr(out), _ptr(residual_out), T, H, float(eps),
-        _stream(stream)))
+        _ptr(x), _ptr(residual), _ptr(weight), _ptr(out), _ptr(residual_out), T, H, stride,
+        float(eps), _stream(stream)))
 
 
 def nv_qknorm_rope(q, k, q_norm_weight, k_norm_weight, cos_sin, positions, eps: float = 1e-6,

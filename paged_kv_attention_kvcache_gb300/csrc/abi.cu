@@ -151,18 +151,19 @@ int nv_rope_cos_sin_cache(float *cos_sin, int max_position, int rotary_dim, doub
 }
 
 int nv_add_rmsnorm(const nv_bf16_t *x, const nv_bf16_t *residual, const nv_bf16_t *weight,
-                   nv_bf16_t *out, nv_bf16_t *residual_out, int64_t T, int H, float eps,
-                   void *stream) {
-    if (T < 0 || T > 0x7FFFFFFF || H <= 0 || !(eps >= 0.f) || !isfinite(eps)) return NV_EINVAL;
+                   nv_bf16_t *out, nv_bf16_t *residual_out, int64_t T, int H,
+                   int64_t row_stride, float eps, void *stream) {
+    if (T < 0 || T > 0x7FFFFFFF || H <= 0 || row_stride < H || !(eps >= 0.f) || !isfinite(eps))
+        return NV_EINVAL;
     if (H % 8 != 0 || H > 16384) return NV_EUNSUPPORTED;
     if (T == 0) return NV_OK;
     if (!x || !weight || !out || (residual && !residual_out)) return NV_EINVAL;
-    if (!aligned16(x) || !aligned16(weight) || !aligned16(out) ||
+    if (row_stride % 8 || !aligned16(x) || !aligned16(weight) || !aligned16(out) ||
         (residual && (!aligned16(residual) || !aligned16(residual_out))))
         return NV_EALIGN;
     return launch_status(launch_add_rmsnorm(x, residual, weight, out,
-                                            residual ? residual_out : nullptr, T, H, eps,
-                                            as_stream(stream)));
+                                            residual ? residual_out : nullptr, T, H, row_stride,
+                                            eps, as_stream(stream)));
 }
 
 int nv_qknorm_rope(nv_bf16_t *q, int64_t q_tok_stride, nv_bf16_t *k, int64_t k_tok_stride,

@@ -48,7 +48,7 @@ cudaError_t launch_rope_cos_sin(float *cos_sin, int max_position, int rotary_dim
 
 cudaError_t launch_add_rmsnorm(const uint16_t *x, const uint16_t *residual,
                                const uint16_t *weight, uint16_t *out, uint16_t *residual_out,
-                               int64_t T, int H, float eps, cudaStream_t s);
+                               int64_t T, int H, int64_t row_stride, float eps, cudaStream_t s);
 
 cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64_t k_stride,
                                const uint16_t *qw, const uint16_t *kw, const float *cos_sin,

@@ -51,10 +51,12 @@ template <int VPT, bool kResidual>
 __global__ void __launch_bounds__(kNormThreads)
 add_rmsnorm_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ residual,
                    const uint4 *__restrict__ weight, uint4 *__restrict__ out,
-                   uint4 *__restrict__ residual_out, int nvec, float inv_h, float eps) {
+                   uint4 *__restrict__ residual_out, int nvec, int64_t vstride, float inv_h,
+                   float eps) {
     pdl_wait_release();
     const int64_t row = blockIdx.x;
-    const uint4 *xr = x + row * nvec;
+    const int64_t row0 = row * vstride;          // first 16-byte vector of the row
+    const uint4 *xr = x + row0;
     float s[VPT][8];
     float sum_sq = 0.f;
 #pragma unroll
@@ -69,7 +71,7 @@ add_rmsnorm_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ residu
                 s[v][2 * e + 1] = bf16_hi(aw[e]);
             }
             if (kResidual) {
-                uint4 r = __ldg(residual + row * nvec + c);
+                uint4 r = __ldg(residual + row0 + c);
                 const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
                 uint32_t o[4];
 #pragma unroll
@@ -78,7 +80,7 @@ add_rmsnorm_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ residu
                     s[v][2 * e + 1] += bf16_hi(rw[e]);
                     o[e] = pack_bf16x2(s[v][2 * e], s[v][2 * e + 1]);
                 }
-                residual_out[row * nvec + c] = make_uint4(o[0], o[1], o[2], o[3]);
+                residual_out[row0 + c] = make_uint4(o[0], o[1], o[2], o[3]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) sum_sq = fmaf(s[v][e], s[v][e], sum_sq);
@@ -104,7 +106,7 @@ add_rmsnorm_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ residu
             for (int e = 0; e < 4; ++e)
                 o[e] = pack_bf16x2(s[v][2 * e] * rstd * bf16_lo(gw[e]),
                                    s[v][2 * e + 1] * rstd * bf16_hi(gw[e]));
-            out[row * nvec + c] = make_uint4(o[0], o[1], o[2], o[3]);
+            out[row0 + c] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
 }
@@ -112,31 +114,34 @@ add_rmsnorm_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ residu
 template <int VPT>
 static cudaError_t launch_norm_vpt(const uint16_t *x, const uint16_t *residual,
                                    const uint16_t *weight, uint16_t *out,
-                                   uint16_t *residual_out, int64_t T, int H, float eps,
-                                   cudaStream_t s) {
+                                   uint16_t *residual_out, int64_t T, int H,
+                                   int64_t row_stride, float eps, cudaStream_t s) {
     const int nvec = H / 8;
+    const int64_t vstride = row_stride / 8;
     const float inv_h = 1.0f / (float)H;
     dim3 grid((unsigned)T);
     if (residual)
         return launch_pdl(add_rmsnorm_kernel<VPT, true>, grid, dim3(kNormThreads), (size_t)0, s,
                           (const uint4 *)x, (const uint4 *)residual, (const uint4 *)weight,
-                          (uint4 *)out, (uint4 *)residual_out, nvec, inv_h, eps);
+                          (uint4 *)out, (uint4 *)residual_out, nvec, vstride, inv_h, eps);
     return launch_pdl(add_rmsnorm_kernel<VPT, false>, grid, dim3(kNormThreads), (size_t)0, s,
                       (const uint4 *)x, (const uint4 *)nullptr, (const uint4 *)weight,
-                      (uint4 *)out, (uint4 *)nullptr, nvec, inv_h, eps);
+                      (uint4 *)out, (uint4 *)nullptr, nvec, vstride, inv_h, eps);
 }
 
 cudaError_t launch_add_rmsnorm(const uint16_t *x, const uint16_t *residual,
                                const uint16_t *weight, uint16_t *out, uint16_t *residual_out,
-                               int64_t T, int H, float eps, cudaStream_t s) {
+                               int64_t T, int H, int64_t row_stride, float eps, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int nvec = H / 8;
     const int vpt = (nvec + kNormThreads - 1) / kNormThreads;
-    if (vpt <= 1) return launch_norm_vpt<1>(x, residual, weight, out, residual_out, T, H, eps, s);
-    if (vpt <= 2) return launch_norm_vpt<2>(x, residual, weight, out, residual_out, T, H, eps, s);
-    if (vpt <= 4) return launch_norm_vpt<4>(x, residual, weight, out, residual_out, T, H, eps, s);
-    if (vpt <= 8) return launch_norm_vpt<8>(x, residual, weight, out, residual_out, T, H, eps, s);
-    return launch_norm_vpt<16>(x, residual, weight, out, residual_out, T, H, eps, s);
+#define NV_NORM_ARGS x, residual, weight, out, residual_out, T, H, row_stride, eps, s
+    if (vpt <= 1) return launch_norm_vpt<1>(NV_NORM_ARGS);
+    if (vpt <= 2) return launch_norm_vpt<2>(NV_NORM_ARGS);
+    if (vpt <= 4) return launch_norm_vpt<4>(NV_NORM_ARGS);
+    if (vpt <= 8) return launch_norm_vpt<8>(NV_NORM_ARGS);
+    return launch_norm_vpt<16>(NV_NORM_ARGS);
+#undef NV_NORM_ARGS
 }
 
 // ------------------------------------------------------- QK-Norm + RoPE

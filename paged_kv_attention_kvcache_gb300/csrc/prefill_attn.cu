@@ -23,8 +23,9 @@
 //    (separate K and V barriers, so QK^T can start before V lands).  Every
 //    tile is stored as two 128-byte-swizzled halves of head_dim, the
 //    canonical layout tcgen05 reads.  Paged: one block-table lookup per key
-//    tile, and the rows past Lk of an item's last V tile are overwritten
-//    with zeros once it lands (cache rows there may hold any bits).
+//    tile.  The rows past Lk of an item's last V tile are overwritten with
+//    zeros once it lands (cache rows there, or the next packed sequence's
+//    rows, may hold any bits) before the tile's full barrier completes.
 //  - Warp 9 allocates all 512 TMEM columns (S_a at 128a, O_a at 256 + 128a
 //    for query tile a).  Warps 9 and 10 issue tcgen05.mma for query tiles 0
 //    and 1: S_a,j = Q_a K_j^T (M = N = 128, bf16 in, fp32 accumulate in
@@ -95,16 +96,17 @@ struct Barriers {
     uint64_t k_empty[kKStages], v_empty[kVStages];
     uint64_t s_full[kQTiles], p_full[kQTiles], o_full[kQTiles], o_empty[kQTiles];
     uint64_t item_full[kItemRing], item_empty[kItemRing];
-    // Paged: one phase per load into V slot s, completed at the load's issue,
-    // or for an item's last tile with rows past Lk once they are zeroed.
-    uint64_t v_clean[kVStages];
+    // An item's last V tile with rows past Lk lands here first; the producer
+    // then overwrites those rows with zeros, and the zeros' arrival completes
+    // the slot's v_full phase.
+    uint64_t v_land[kVStages];
     Item item[kItemRing];       // decoded items; n_kv < 0 = no more work
     uint32_t tmem_base;
     int failed;
 };
 
-// Zeros copied over the rows past Lk of a paged item's last V tile (one
-// 64-dim half: at most 127 rows of 128 bytes).
+// Zeros copied over the rows past Lk of an item's last V tile (one 64-dim
+// half: at most 127 rows of 128 bytes).
 __device__ __align__(128) uint8_t g_zero_rows[kHalf];
 
 // The work list: every non-empty (query-tile pair, sequence), heaviest first.
@@ -452,7 +454,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&bars->item_full[r], 1);
             mbar_init(&bars->item_empty[r], kItemReaders);
         }
-        for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_clean[s], 1);
+        for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_land[s], 1);
         bars->failed = 0;
         fence_mbarrier_init();
     }
@@ -519,16 +521,44 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 ++kcnt;
                 return true;
             };
+            // Rows past Lk of an item's last V tile may hold any bits: cache
+            // rows of no sequence (paged), or the next packed sequence's rows
+            // (contiguous).  Their probability is zero, but 0 * NaN is not.
+            // Such a tile lands on v_land; once the next item's Q and first K
+            // loads are out (by then it has normally landed) the rows past Lk
+            // are overwritten by two bulk copies of zeros from global memory,
+            // and the zeros' arrival completes the slot's v_full phase, so the
+            // MMA warps wait exactly as for any other tile.
+            int zslot = -1, ztail = 0;
+            uint32_t land_parity = 0;        // bit s: parity of v_land[s]'s next phase
             auto load_v = [&](const Item &it, int j) {
                 const int st = vcnt % kVStages;
                 if (vcnt >= kVStages &&
                     !mbar_wait(&bars->v_empty[st], ((vcnt / kVStages) - 1) & 1))
                     return false;
-                mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-                load_tile(&v_map, smem + kOffV + st * kTileBytes, &bars->v_full[st], it, j);
-                if (kPaged && !(j == it.n_kv - 1 && it.Lk - j * kBN < kBN))
-                    mbar_arrive(&bars->v_clean[st]);      // nothing to zero in this tile
+                const int tail = it.Lk - j * kBN;
+                uint64_t *bar = &bars->v_full[st];
+                if (j == it.n_kv - 1 && tail < kBN) {
+                    bar = &bars->v_land[st];
+                    zslot = st;
+                    ztail = tail;
+                }
+                mbar_arrive_expect_tx(bar, kTileBytes);
+                load_tile(&v_map, smem + kOffV + st * kTileBytes, bar, it, j);
                 ++vcnt;
+                return true;
+            };
+            auto zero_tail = [&]() {
+                const int st = zslot;
+                zslot = -1;
+                const uint32_t par = (land_parity >> st) & 1u;
+                land_parity ^= 1u << st;
+                if (!mbar_wait(&bars->v_land[st], par)) return false;
+                uint8_t *sV = smem + kOffV + st * kTileBytes;
+                const uint32_t bytes = (uint32_t)(kBN - ztail) * 128u;
+                mbar_arrive_expect_tx(&bars->v_full[st], 2 * bytes);
+                bulk_load(sV + ztail * 128, g_zero_rows, bytes, &bars->v_full[st]);
+                bulk_load(sV + kHalf + ztail * 128, g_zero_rows, bytes, &bars->v_full[st]);
                 return true;
             };
             // Items are decoded here once and published, whole, through the
@@ -581,36 +611,16 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 ++qcnt;
                 ok = load_k(it, 0);
+                if (ok && zslot >= 0) ok = zero_tail();      // the previous item's last V
                 for (int j = 0; ok && j < it.n_kv; ++j) {
                     if (j + 1 < it.n_kv) ok = load_k(it, j + 1);
                     if (ok) ok = load_v(it, j);
                 }
                 if (!ok) break;
-                // Paged: rows past Lk of the item's last V tile (slot `zc`) are
-                // zeroed once the next item has been drawn (the atomic's latency
-                // overlaps the tile's landing).
-                const int ztail = kPaged ? it.Lk - (it.n_kv - 1) * kBN : kBN;
-                const int zc = vcnt - 1;
                 fetch(it);
                 ok = publish(it);
-                if (ok && kPaged && ztail < kBN) {
-                    // Cache rows past Lk may hold any bits; their probability is
-                    // zero but 0 * NaN is not.  Once the tile has landed, its rows
-                    // past Lk are overwritten by two bulk copies of zeros from
-                    // global memory (async proxy, like the tile's own load: no
-                    // proxy fence), signalled on v_clean.
-                    if (!mbar_wait(&bars->v_full[zc % kVStages], (zc / kVStages) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *sV = smem + kOffV + (zc % kVStages) * kTileBytes;
-                    const uint32_t bytes = (uint32_t)(kBN - ztail) * 128u;
-                    uint64_t *vc = &bars->v_clean[zc % kVStages];
-                    mbar_arrive_expect_tx(vc, 2 * bytes);
-                    bulk_load(sV + ztail * 128, g_zero_rows, bytes, vc);
-                    bulk_load(sV + kHalf + ztail * 128, g_zero_rows, bytes, vc);
-                }
             }
+            if (ok && zslot >= 0) ok = zero_tail();          // the last item's last V
             if (!ok) record_failure(bars, p.err_count);
         }
     } else if (warp >= kMmaWarp) {
@@ -644,15 +654,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             const int last1 = itr.last[1];
             // (a select, not itr.last[a]: one load either way)
             const int last = a ? last1 : itr.last[0];
-            const int Lk = itr.Lk;
             const bool has1 = last1 >= 0;
             // Key tile j of this item is ring slot kbase + j (same for V).
             const int kbase = kcnt, vbase = vcnt;
             kcnt += n_kv;
             vcnt += n_kv;
-            // Paged: first row past Lk in the item's last key tile (-1: none).
-            const int tail = Lk - (n_kv - 1) * kBN;
-            const int zero_from = (kPaged && tail < kBN) ? tail : -1;
             int k_ready = -1, v_ready = -1;
             auto ensure_k = [&](int j) {
                 if (ok && k_ready < j) {
@@ -723,12 +729,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (j + 1 <= last) ensure_k(j + 1);
                 if (ok && j == 0 && ocnt >= 1)        // epilogue of the previous item done
                     ok = wait_all(&bars->o_empty[a], (ocnt - 1) & 1);
-                if (kPaged && ok && zero_from >= 0 && j == n_kv - 1)
-                    // The producer zeroes the last tile's rows past Lk; a PV
-                    // reading the tile waits for that (before P, to keep the
-                    // round trip off the softmax -> PV chain).
-                    ok = wait_all(&bars->v_clean[(vbase + j) % kVStages],
-                                  ((vbase + j) / kVStages) & 1);
                 if (ok) ok = wait_all(&bars->p_full[a], pcnt & 1);
                 if (!ok) return;
                 ++pcnt;

@@ -57,13 +57,15 @@ MIS = 0x10002           # misaligned
 
 def test_add_rmsnorm_rejects_bad_arguments(lib):
     f = lib.nv_add_rmsnorm
-    assert f(None, None, FAKE, FAKE, None, 4, 1024, 1e-6, None) == NV_EINVAL
-    assert f(FAKE, None, FAKE, FAKE, None, -1, 1024, 1e-6, None) == NV_EINVAL
-    assert f(FAKE, None, FAKE, FAKE, None, 4, 1020, 1e-6, None) == NV_EUNSUPPORTED
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 4, 1024, 1e-6, None) == NV_EINVAL   # residual_out missing
-    assert f(MIS, None, FAKE, FAKE, None, 4, 1024, 1e-6, None) == NV_EALIGN
-    assert f(FAKE, None, FAKE, FAKE, None, 0, 1024, 1e-6, None) == NV_OK      # empty: no-op
-    assert f(FAKE, None, FAKE, FAKE, None, 4, 1024, float("nan"), None) == NV_EINVAL
+    assert f(None, None, FAKE, FAKE, None, 4, 1024, 1024, 1e-6, None) == NV_EINVAL
+    assert f(FAKE, None, FAKE, FAKE, None, -1, 1024, 1024, 1e-6, None) == NV_EINVAL
+    assert f(FAKE, None, FAKE, FAKE, None, 4, 1020, 1020, 1e-6, None) == NV_EUNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 4, 1024, 1024, 1e-6, None) == NV_EINVAL  # no residual_out
+    assert f(MIS, None, FAKE, FAKE, None, 4, 1024, 1024, 1e-6, None) == NV_EALIGN
+    assert f(FAKE, None, FAKE, FAKE, None, 0, 1024, 1024, 1e-6, None) == NV_OK     # empty: no-op
+    assert f(FAKE, None, FAKE, FAKE, None, 4, 1024, 1024, float("nan"), None) == NV_EINVAL
+    assert f(FAKE, None, FAKE, FAKE, None, 4, 1024, 1000, 1e-6, None) == NV_EINVAL  # stride < H
+    assert f(FAKE, None, FAKE, FAKE, None, 4, 1024, 1028, 1e-6, None) == NV_EALIGN  # stride % 8
 
 
 def test_qknorm_rope_rejects_bad_arguments(lib):

@@ -134,6 +134,29 @@ def test_add_rmsnorm_decode_step_8b():
     _norm_case(x, r, gamma)
 
 
+def test_add_rmsnorm_strided_rows():
+    # Rows that are views into wider buffers (row stride 1024 + 64 elements):
+    # each of x, residual, out and residual_out is [T, 1024] with the same
+    # stride; the padding between rows must stay untouched.
+    g = np.random.default_rng(29)
+    T, H, pad = 37, 1024, 64
+    x = wl.f32_to_bf16_bits(g.standard_normal((T, H)).astype(np.float32))
+    r = wl.f32_to_bf16_bits(g.standard_normal((T, H)).astype(np.float32))
+    gamma = wl.f32_to_bf16_bits((1 + 0.1 * g.standard_normal(H)).astype(np.float32))
+    fill = np.full((T, pad), 0x3F80, np.uint16)                 # 1.0 in the gaps
+    xb, rb = dev(np.concatenate([x, fill], 1)), dev(np.concatenate([r, fill], 1))
+    ob = dev(np.concatenate([np.zeros_like(x), fill], 1))
+    rob = dev(np.concatenate([np.zeros_like(x), fill], 1))
+    nv.nv_add_rmsnorm(xb[:, :H], rb[:, :H], dev(gamma), ob[:, :H], rob[:, :H], eps=wl.RMS_EPS)
+    torch.cuda.synchronize()
+    y_ref, r_ref = oracle.add_rmsnorm(x, r, gamma, wl.RMS_EPS)
+    check_close(host(ob)[:, :H], y_ref, "add_rmsnorm strided out")
+    check_close(host(rob)[:, :H], r_ref, "add_rmsnorm strided residual", max_tol=2 ** -8,
+                mean_tol=2 ** -9)
+    for buf in (ob, rob):
+        assert np.all(host(buf)[:, H:] == 0x3F80), "padding between rows was written"
+
+
 def test_add_rmsnorm_in_place_residual():
     g = np.random.default_rng(23)
     x = wl.f32_to_bf16_bits(g.standard_normal((33, 1024)).astype(np.float32))

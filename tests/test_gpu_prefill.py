@@ -113,6 +113,26 @@ def test_prefill_qwen3_8b_batch_full_size():
     check_close(got, ref, "prefill cfg4 (16 seqs, 33k tokens, 32/8 heads)")
 
 
+def test_prefill_neighbouring_sequence_nan_rows_do_not_leak():
+    # Packed sequences share 128-row key tiles: the last tile of a sequence
+    # reads the next sequence's rows, masked.  With NaN in every K and V row
+    # of the middle sequence, the other sequences' outputs must still be the
+    # oracle's (their masked keys carry probability 0, and 0 * NaN is not 0,
+    # so those V rows must be cleared before use).  Both schedules.
+    hq, hkv = 8, 2
+    lengths = np.array([100, 70, 300, 1, 129])
+    T = int(lengths.sum())
+    qkv = wl.normal_bf16(535, "prefill.nan", (T, (hq + 2 * hkv) * 128))
+    cu = wl.cu_seqlens(lengths)
+    qkv[cu[1]:cu[2], hq * 128:] = 0x7FC0          # K and V rows of sequence 1: NaN
+    q, k, v = split_qkv(qkv, hq, hkv)
+    keep = np.r_[cu[0]:cu[1], cu[2]:cu[5]]
+    for dynamic in (True, False):
+        got = run_prefill(qkv, lengths, hq, hkv, dynamic)
+        ref = oracle.attention_varlen(q, k, v, cu, cu, SCALE, True)
+        check_close(got[keep], ref[keep], f"prefill next to NaN rows dynamic={dynamic}")
+
+
 # ------------------------------------------- keys beyond the queries (prefix)
 def test_prefill_contiguous_keys_with_prefix():
     # Each sequence's keys are a prefix followed by its Lq new tokens; query i
