@@ -52,11 +52,11 @@ SCALE = 128 ** -0.5
 # ncu capture of `bench.py --ncu-case decode` (reads + writes of
 # decode_split_kernel over its algorithmic bytes), valid only for the kernel
 # code it was taken on (the hash ignores comments and layout).
-DECODE_TRAFFIC = {"ratio": 1.0032, "source_sha256_16": "c016c1bf02d2a4c9"}
+DECODE_TRAFFIC = {"ratio": 1.0035, "source_sha256_16": "20ea38edbcf31527"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1056003456, "source_sha256_16": "3b39ece31c628a8d"}
+PREFILL_TRAFFIC = {"bytes": 1048043264, "source_sha256_16": "15956090669d9189"}
 
 
 def max_over_ranks(values, world: int, device=None):
@@ -1044,7 +1044,27 @@ def run_ncu_case(which: str, launches: int = 3):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
             torch.bfloat16).cuda()
 
-    if which == "decode":
+    if which == "decode-small":
+        # The Qwen3-0.6B-head set as measured (B = 64, ctx U[512, 4096], 0.6 GB of
+        # K/V, automatic split): store_kvcache of the new tokens, then decode.
+        step = wl.config2()
+        s = step.shape
+        B, Q, D = step.context_lens.size, s.q_size, s.kv_size
+        qkv = dev(step.qkv)
+        q = qkv[:, :Q].view(B, s.hq, 128)
+        k = qkv[:, Q:Q + D].view(B, s.hkv, 128)
+        v = qkv[:, Q + D:].view(B, s.hkv, 128)
+        kc, vc = dev(step.pool.k), dev(step.pool.v)
+        bt = torch.from_numpy(step.block_tables).cuda()
+        cl = torch.from_numpy(step.context_lens).cuda()
+        slots = torch.from_numpy(step.slot_mapping).cuda()
+        o = torch.empty(B, s.hq, 128, dtype=torch.bfloat16, device="cuda")
+        ws_b = nv.nv_decode_attn_workspace_size(B, s.hq, s.hkv, 128, bt.shape[1], 256, 0)
+        ws = torch.empty(max(1, ws_b // 4), dtype=torch.float32, device="cuda")
+        for _ in range(launches):
+            nv.nv_store_kvcache(k, v, kc, vc, slots)
+            nv.nv_decode_attn_paged(q, kc, vc, bt, cl, o, SCALE, workspace=ws)
+    elif which == "decode":
         # Qwen3-8B heads, 64 sequences of 8192 keys: 2.1 GB of K/V, split as the
         # bench's decode step is (2048 keys).
         ctx = np.full(64, 8192, np.int32)
@@ -1134,7 +1154,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill", "layer"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "decode-small", "prefill", "layer"],
+                    default=None,
                     help="run a small case of one kernel, or every prefill-layer kernel on the "
                          "bench batch (for ncu captures), and exit")
     args = ap.parse_args()

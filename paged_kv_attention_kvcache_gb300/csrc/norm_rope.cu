@@ -306,11 +306,17 @@ cudaError_t launch_qknorm_rope(uint16_t *q, int64_t q_stride, uint16_t *k, int64
 // the order: rotate q and k, then write k and v to their slots).  A token owns
 // Hq + 2 Hkv rows of 128 elements: q rows are rotated in place, k rows are
 // rotated and written to the token's cache slot (and back in place only when
-// asked), v rows are copied bit for bit to the slot.  Eight lanes per row as
-// above; k never makes the extra round trip through HBM that the separate
-// store kernel would read it back for.
+// asked), v rows are copied bit for bit to the slot.  k never makes the extra
+// round trip through HBM that the separate store kernel would read it back
+// for.  Two phases, each with the grid's stride:
+//  - the q and k rows, eight lanes per row as above;
+//  - the v rows, one warp per token, all of the token's 16-byte loads issued
+//    before its stores (the copy pattern of store_kvcache_kernel, which keeps
+//    more bytes in flight than the rotation's row groups do).
 // Four blocks per SM (64 registers, a few bytes spilled) measured faster
 // than three without the spill: the loads in flight per SM are what count.
+constexpr int kVCopyMaxVecPerLane = 8;    // D <= 2048 in one pass
+
 __global__ void __launch_bounds__(kRopeThreads, 4)
 qknorm_rope_store_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *__restrict__ k,
                          int64_t k_stride, const uint16_t *__restrict__ v, int64_t v_stride,
@@ -321,80 +327,98 @@ qknorm_rope_store_kernel(uint16_t *__restrict__ q, int64_t q_stride, uint16_t *_
                          uint16_t *__restrict__ v_cache, int64_t num_slots, int64_t T, int Hq,
                          int Hkv, float eps, int write_k, int *err_count) {
     pdl_wait_release();
-    const int heads = Hq + 2 * Hkv;
+    const int heads = Hq + Hkv;                   // rows of the rotation phase per token
     const int64_t n_rows = T * heads;
     const int lane = threadIdx.x & 31;
     const int j = lane & 7;
     const int64_t groups = (int64_t)gridDim.x * (kRopeThreads / 8);
     const int64_t D = (int64_t)Hkv * 128;
-    int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
-    if (row >= n_rows) return;
     const unsigned gmask = 0xFFu << (lane & ~7);
-    // Grid-stride over rows as in qknorm_rope_kernel: the next row's vectors,
-    // position and slot are in flight while the current row is processed.
-    auto source = [&](int64_t t, int h) -> uint16_t * {
-        if (h < Hq) return q + t * q_stride + (int64_t)h * 128;
-        if (h < Hq + Hkv) return k + t * k_stride + (int64_t)(h - Hq) * 128;
-        return const_cast<uint16_t *>(v) + t * v_stride + (int64_t)(h - Hq - Hkv) * 128;
-    };
-    int64_t t = row / heads;
-    int h = (int)(row - t * heads);
-    uint16_t *base = source(t, h);
-    uint4 a = *reinterpret_cast<const uint4 *>(base + 8 * j);
-    uint4 b = *reinterpret_cast<const uint4 *>(base + 64 + 8 * j);
-    int64_t pos = __ldg(positions + t);
-    int64_t slot = h >= Hq ? (int64_t)__ldg(slot_mapping + t) : -1;
-    for (;;) {
-        const int64_t next = row + groups;
-        const bool more = next < n_rows;
-        int64_t nt = t, npos = pos, nslot = slot;
-        int nh = h;
-        uint16_t *nbase = base;
-        uint4 na = a, nb = b;
-        if (more) {
-            nt = next / heads;
-            nh = (int)(next - nt * heads);
-            nbase = source(nt, nh);
-            na = *reinterpret_cast<const uint4 *>(nbase + 8 * j);
-            nb = *reinterpret_cast<const uint4 *>(nbase + 64 + 8 * j);
-            npos = __ldg(positions + nt);
-            nslot = nh >= Hq ? (int64_t)__ldg(slot_mapping + nt) : -1;
-        }
-        if (slot != -1 && (slot < 0 || slot >= num_slots)) {
-            if (j == 0 && h == Hq) count_error(err_count);   // once per token
-            slot = -1;
-        }
-        if (h >= Hq + Hkv) {                                    // v: a bit copy
-            if (slot >= 0) {
-                uint16_t *dst = v_cache + slot * D + (int64_t)(h - Hq - Hkv) * 128;
-                *reinterpret_cast<uint4 *>(dst + 8 * j) = a;
-                *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = b;
+    // ---- phase 1: q and k rows.  Grid-stride over rows as in
+    // qknorm_rope_kernel: the next row's vectors, position and slot are in
+    // flight while the current row is processed.
+    int64_t row = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 3;
+    if (row < n_rows) {
+        auto source = [&](int64_t t, int h) -> uint16_t * {
+            return h < Hq ? q + t * q_stride + (int64_t)h * 128
+                          : k + t * k_stride + (int64_t)(h - Hq) * 128;
+        };
+        int64_t t = row / heads;
+        int h = (int)(row - t * heads);
+        uint16_t *base = source(t, h);
+        uint4 a = *reinterpret_cast<const uint4 *>(base + 8 * j);
+        uint4 b = *reinterpret_cast<const uint4 *>(base + 64 + 8 * j);
+        int64_t pos = __ldg(positions + t);
+        int64_t slot = h >= Hq ? (int64_t)__ldg(slot_mapping + t) : -1;
+        for (;;) {
+            const int64_t next = row + groups;
+            const bool more = next < n_rows;
+            int64_t nt = t, npos = pos, nslot = slot;
+            int nh = h;
+            uint16_t *nbase = base;
+            uint4 na = a, nb = b;
+            if (more) {
+                nt = next / heads;
+                nh = (int)(next - nt * heads);
+                nbase = source(nt, nh);
+                na = *reinterpret_cast<const uint4 *>(nbase + 8 * j);
+                nb = *reinterpret_cast<const uint4 *>(nbase + 64 + 8 * j);
+                npos = __ldg(positions + nt);
+                nslot = nh >= Hq ? (int64_t)__ldg(slot_mapping + nt) : -1;
             }
-        } else if (pos < 0 || pos >= max_position) {
-            if (j == 0) count_error(err_count);
-        } else {
-            const bool is_q = h < Hq;
-            uint4 o1, o2;
-            norm_rope_regs(a, b, is_q ? qw : kw, cos_sin + pos * 128, j, gmask, eps, o1, o2);
-            if (is_q || write_k) {
-                *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
-                *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
+            if (slot != -1 && (slot < 0 || slot >= num_slots)) {
+                if (j == 0 && h == Hq) count_error(err_count);   // once per token
+                slot = -1;
             }
-            if (!is_q && slot >= 0) {
-                uint16_t *dst = k_cache + slot * D + (int64_t)(h - Hq) * 128;
-                *reinterpret_cast<uint4 *>(dst + 8 * j) = o1;
-                *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = o2;
+            if (pos < 0 || pos >= max_position) {
+                if (j == 0) count_error(err_count);
+            } else {
+                const bool is_q = h < Hq;
+                uint4 o1, o2;
+                norm_rope_regs(a, b, is_q ? qw : kw, cos_sin + pos * 128, j, gmask, eps, o1, o2);
+                if (is_q || write_k) {
+                    *reinterpret_cast<uint4 *>(base + 8 * j) = o1;
+                    *reinterpret_cast<uint4 *>(base + 64 + 8 * j) = o2;
+                }
+                if (!is_q && slot >= 0) {
+                    uint16_t *dst = k_cache + slot * D + (int64_t)(h - Hq) * 128;
+                    *reinterpret_cast<uint4 *>(dst + 8 * j) = o1;
+                    *reinterpret_cast<uint4 *>(dst + 64 + 8 * j) = o2;
+                }
+            }
+            if (!more) break;
+            row = next;
+            t = nt;
+            h = nh;
+            base = nbase;
+            a = na;
+            b = nb;
+            pos = npos;
+            slot = nslot;
+        }
+    }
+    // ---- phase 2: v rows, a bit copy (a bad slot was counted in phase 1).
+    const int vec = (int)(D / 8);
+    const int64_t warps = (int64_t)gridDim.x * (kRopeThreads / 32);
+    const uint4 *vv = reinterpret_cast<const uint4 *>(v);
+    uint4 *vc = reinterpret_cast<uint4 *>(v_cache);
+    for (int64_t t = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 5; t < T; t += warps) {
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0 || slot >= num_slots) continue;
+        const uint4 *src = vv + t * (v_stride / 8);
+        for (int c0 = 0; c0 < vec; c0 += 32 * kVCopyMaxVecPerLane) {
+            uint4 x[kVCopyMaxVecPerLane];
+#pragma unroll
+            for (int u = 0; u < kVCopyMaxVecPerLane; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < vec) x[u] = __ldg(src + c);
+            }
+#pragma unroll
+            for (int u = 0; u < kVCopyMaxVecPerLane; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < vec) vc[slot * vec + c] = x[u];
             }
         }
-        if (!more) break;
-        row = next;
-        t = nt;
-        h = nh;
-        base = nbase;
-        a = na;
-        b = nb;
-        pos = npos;
-        slot = nslot;
     }
 }
 
@@ -406,7 +430,7 @@ cudaError_t launch_qknorm_rope_store(uint16_t *q, int64_t q_stride, uint16_t *k,
                                      uint16_t *k_cache, uint16_t *v_cache, int64_t num_slots,
                                      int64_t T, int Hq, int Hkv, float eps, int write_k,
                                      int *err_count, cudaStream_t s) {
-    const int64_t rows = T * (Hq + 2 * Hkv);
+    const int64_t rows = T * (Hq + Hkv);
     if (rows == 0) return cudaSuccess;
     const int64_t threads = rows * 8;
     static const int64_t resident = resident_grid(qknorm_rope_store_kernel, kRopeThreads, 4);
