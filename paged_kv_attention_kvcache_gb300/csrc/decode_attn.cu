@@ -327,43 +327,63 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const DecodeParams p) {
     pdl_wait_release();
+    const int64_t wid = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool valid = wid < (int64_t)p.B * p.Hq;
+    // The context length is requested before the failure flag is read, so
+    // the two round trips overlap.
+    int L = valid ? __ldg(p.context_lens + wid / p.Hq) : 0;
     // After a pipeline failure (this call's or an earlier one's, bit 30 of
     // err_count) some splits wrote nothing: their workspace slots may hold an
     // earlier call's partials.  Merge nothing and leave o as it is, as the
     // split kernel does for the sequences it did not process.
     if (pipeline_failed_before(p.err_count)) return;
-    const int64_t wid = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= (int64_t)p.B * p.Hq) return;
-    const int b = (int)(wid / p.Hq);
+    if (!valid) return;
     const int max_l = p.max_blocks * p.block_size;
-    int L = __ldg(p.context_lens + b);
     L = L < 0 ? 0 : (L > max_l ? max_l : L);
     const int n_splits = (L + p.split_tokens - 1) / p.split_tokens;
     if (n_splits <= 1) return;                  // written by the split kernel
     const float *lse = p.ws_lse + wid * p.max_splits;
+    const float4 *part = reinterpret_cast<const float4 *>(p.ws_o + wid * p.max_splits * 128) + lane;
     float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, lse[s]);
-    if (M == -INFINITY) {                       // every key of the sequence was skipped
-        *reinterpret_cast<uint2 *>(p.o + wid * 128 + 4 * lane) = make_uint2(0u, 0u);
-        return;
-    }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float den = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-        // A split whose keys were all skipped has lse = -inf and weight 0.
-        const float f = lse[s] == -INFINITY ? 0.f : fast_exp2(lse[s] - M);
-        const float4 v = *reinterpret_cast<const float4 *>(p.ws_o + (wid * p.max_splits + s) * 128 + 4 * lane);
+    // A split whose keys were all skipped has lse = -inf and weight 0.
+    auto add = [&](float ls, float4 v) {
+        const float f = ls == -INFINITY ? 0.f : fast_exp2(ls - M);
         acc[0] = fmaf(f, v.x, acc[0]);
         acc[1] = fmaf(f, v.y, acc[1]);
         acc[2] = fmaf(f, v.z, acc[2]);
         acc[3] = fmaf(f, v.w, acc[3]);
         den += f;
+    };
+    constexpr int kInFlight = 8;
+    if (n_splits <= kInFlight) {
+        // Every load of the merge in one round trip.
+        float ls[kInFlight];
+        float4 v[kInFlight];
+#pragma unroll
+        for (int s = 0; s < kInFlight; ++s) {
+            ls[s] = s < n_splits ? lse[s] : -INFINITY;
+            v[s] = s < n_splits ? part[s * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int s = 0; s < kInFlight; ++s) M = fmaxf(M, ls[s]);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int s = 0; s < kInFlight; ++s) add(ls[s], v[s]);
+        }
+    } else {
+        for (int s = 0; s < n_splits; ++s) M = fmaxf(M, lse[s]);
+        if (M != -INFINITY)
+            for (int s = 0; s < n_splits; ++s) add(lse[s], part[s * 32]);
     }
-    const float inv = 1.f / den;
-    uint2 out;
-    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    uint2 out = make_uint2(0u, 0u);             // every key of the sequence skipped
+    if (M != -INFINITY) {
+        const float inv = 1.f / den;
+        out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    }
     *reinterpret_cast<uint2 *>(p.o + wid * 128 + 4 * lane) = out;
 }
 
