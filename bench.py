@@ -50,9 +50,10 @@ SCALE = 128 ** -0.5
 
 # DRAM bytes per algorithmic byte of the decode attention kernels, from an
 # ncu capture of `bench.py --ncu-case decode` (reads + writes of
-# decode_split_kernel over its algorithmic bytes), valid only for the kernel
-# code it was taken on (the hash ignores comments and layout).
-DECODE_TRAFFIC = {"ratio": 1.0035, "source_sha256_16": "20ea38edbcf31527"}
+# decode_split_kernel and decode_merge_kernel over the algorithmic bytes),
+# valid only for the kernel code it was taken on (the hash ignores comments
+# and layout).
+DECODE_TRAFFIC = {"ratio": 1.0036, "source_sha256_16": "ee2678ee523db987"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
