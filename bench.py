@@ -687,7 +687,10 @@ def prefill_prefix_config(dev_t, reps: int = 20):
 # ------------------------------------------ launch overhead: CUDA graph
 def graph_decode_overhead(dev_t, buckets=(1, 8, 64, 512), ctx_len: int = 1024, reps: int = 100):
     """The decode layer's four ABI calls (Qwen3-8B heads) timed eagerly and as
-    one captured CUDA graph per batch bucket.  Every sequence has ctx_len keys;
+    one captured CUDA graph per batch bucket, two ways: back to back (CUDA
+    events over `reps` steps; eager steps then overlap through programmatic
+    launch) and one step at a time with a read-back of the output (host clock;
+    what a serving loop sees per step).  Every sequence has ctx_len keys;
     buckets above 2 end with two padded rows (slot -1, context length 0)."""
     import torch
     import paged_kv_attention_kvcache_gb300 as nv
@@ -758,10 +761,35 @@ def graph_decode_overhead(dev_t, buckets=(1, 8, 64, 512), ctx_len: int = 1024, r
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) * 1e3 / reps
 
+        # One step at a time, as a serving loop runs it: launch the step, read
+        # a few of its outputs back to the host and wait for them; host wall
+        # clock, median.  Host launch cost and the step's full latency count
+        # here; nothing overlaps across steps.
+        host_o = torch.empty(8, dtype=torch.bfloat16).pin_memory()
+        cur = torch.cuda.current_stream()
+
+        def one_step(fn):
+            fn()
+            host_o.copy_(o.view(-1)[:8], non_blocking=True)
+            cur.synchronize()
+
+        def latency(fn, n=200):
+            for _ in range(10):
+                one_step(fn)
+            ts = []
+            for _ in range(n):
+                t = time.perf_counter()
+                one_step(fn)
+                ts.append(time.perf_counter() - t)
+            return statistics.median(ts) * 1e6
+
         eager_us = timed(layer)
         graph_us = timed(graph.replay)
         out.append({"bucket": b, "real": n_real, "eager_us": round(eager_us, 2),
-                    "graph_us": round(graph_us, 2), "kernels": 4 + (1 if wsb else 0)})
+                    "graph_us": round(graph_us, 2),
+                    "eager_step_sync_us": round(latency(layer), 2),
+                    "graph_step_sync_us": round(latency(graph.replay), 2),
+                    "kernels": 4 + (1 if wsb else 0)})
         del graph
     return {"ctx": ctx_len, "heads": "32/8", "per_bucket": out}
 
