@@ -8,12 +8,16 @@
 // inside each; keys of other sequences are never admitted.
 //
 // How (GB300):
-//  - Persistent: one CTA per SM walks work items, an item being a pair of
-//    adjacent 128-row query tiles of one query head of one sequence, so
-//    every K/V tile loaded serves 256 query rows.  Items are numbered
-//    heaviest first: each CTA sorts the non-empty (pair, sequence) entries by
-//    the number of key tiles the pair's last row reads (then sequence, then
-//    pair), and item t * Hq + h is entry t, head h.  With a work counter
+//  - Persistent: one CTA per SM walks work items, an item being two 128-row
+//    query tiles of one sequence that read the same K/V tiles, so every K/V
+//    tile loaded serves 256 query rows.  When the query heads of a kv head
+//    come in even groups the two tiles are heads 2i and 2i + 1 at the same
+//    rows: both read exactly the same key tiles, mask alike and finish
+//    together, and no item is left with a single tile.  Otherwise they are
+//    adjacent row tiles of one head.  Items are numbered heaviest first: each
+//    CTA sorts the non-empty (row unit, sequence) entries by the number of
+//    key tiles the unit's last row reads (then sequence, then unit), and item
+//    t * heads + h is entry t, head (pair) h.  With a work counter
 //    the TMA lane takes the next number from it (atomicAdd), so CTAs that
 //    drew light items take more of them; without one, CTA c takes items c,
 //    c + grid, ...  Either way the number is handed to the other warps
@@ -77,15 +81,20 @@ constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max 
 constexpr int kItemRing = 4;                    // item numbers in flight between the roles
 constexpr int kItemReaders = kQTiles * 5;       // the MMA warps and every softmax warp
 
-// One unit of work: a pair of 128-row query tiles of one head of one
-// sequence.  Items are numbered heaviest first (key tiles read, then
-// sequence, then pair, then head, so the heads sharing a kv head are
-// adjacent).
+// One unit of work: two 128-row query tiles of one sequence that read the
+// same K/V tiles.  When the query heads of a kv head come in even groups,
+// the two tiles are heads 2i and 2i + 1 at the same rows ("head pairs"):
+// both read exactly the same key tiles and mask alike.  Otherwise they are
+// adjacent row tiles of one head, the second reading one key tile more.
+// Items are numbered heaviest first (key tiles read, then sequence, then row
+// unit, then head, so the heads sharing a kv head are adjacent).
 // A sequence has Lq queries and Lk >= Lq keys; query i sits at key position
 // off + i with off = Lk - Lq (causality aligned to the last key: off = 0 for
 // a plain prefill, the cached prefix length for a prefix hit or a chunk).
 struct Item {
-    int h, b, q_start, L, Lk, off, k_start, q0, kvh;
+    int b, q_start, L, Lk, off, k_start, kvh;
+    int qa[kQTiles];        // first row of query tile a within the sequence
+    int ha[kQTiles];        // query head of tile a
     int last[kQTiles];      // last key tile of query tile a (-1: tile has no rows)
     int mask_from[kQTiles]; // first key tile that can hold keys after some row
     int n_kv;               // key tiles the pair needs
@@ -110,7 +119,13 @@ struct Barriers {
 // half: at most 127 rows of 128 bytes).
 __device__ __align__(128) uint8_t g_zero_rows[kHalf];
 
-// The work list: every non-empty (query-tile pair, sequence), heaviest first.
+// Query rows per row unit of the work list: one tile with head pairs, two
+// adjacent tiles otherwise.
+__host__ __device__ __forceinline__ bool use_head_pairs(int Hq, int Hkv) {
+    return (Hq / Hkv) % 2 == 0;
+}
+
+// The work list: every non-empty (row unit, sequence), heaviest first.
 // Numbering every (pair, sequence, head) up to the longest sequence leaves
 // most early numbers empty (short sequences have no high pairs), and each
 // empty number costs the producer a round trip to the work counter; the
@@ -132,8 +147,10 @@ struct Sched {
 // malformed (Lk < Lq), in which case no role touches it.
 __device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n_pairs,
                                             const Sched *sch, Item &it, bool *bad = nullptr) {
-    const int h = w % p.Hq;
-    const int t = w / p.Hq;
+    const bool hp = use_head_pairs(p.Hq, p.Hkv);
+    const int heads = hp ? p.Hq / 2 : p.Hq;          // items per row unit
+    const int h = w % heads;
+    const int t = w / heads;
     int b, pair;
     if (sch->compact) {
         const uint32_t e = sch->key[t];
@@ -145,7 +162,7 @@ __device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n
     }
     const int q_start = __ldg(p.cu_seqlens_q + b);
     const int L = __ldg(p.cu_seqlens_q + b + 1) - q_start;
-    const int q0 = pair * kQTiles * kBM;
+    const int q0 = pair * (hp ? kBM : kQTiles * kBM);
     if (q0 >= L) return false;
     const int k_start = __ldg(p.cu_seqlens_k + b);
     int Lk = __ldg(p.cu_seqlens_k + b + 1) - k_start;
@@ -156,18 +173,18 @@ __device__ __forceinline__ bool decode_item(int w, const PrefillParams &p, int n
     }
     const int off = Lk - L;
     const int nk = (Lk + kBN - 1) / kBN;
-    it.h = h;
     it.b = b;
     it.q_start = q_start;
     it.L = L;
     it.Lk = Lk;
     it.off = off;
     it.k_start = k_start;
-    it.q0 = q0;
-    it.kvh = h / (p.Hq / p.Hkv);
+    it.kvh = (hp ? 2 * h : h) / (p.Hq / p.Hkv);
     it.n_kv = 0;
     for (int a = 0; a < kQTiles; ++a) {
-        const int qa = q0 + a * kBM;
+        const int qa = hp ? q0 : q0 + a * kBM;
+        it.qa[a] = qa;
+        it.ha[a] = hp ? 2 * h + a : h;
         if (qa >= L) {
             it.last[a] = -1;
             it.mask_from[a] = 0;
@@ -228,19 +245,20 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     {
         const int B = p.B;
         const int tid = threadIdx.x;
-        // Pair count of sequence b, and the key tiles pair `pr` of it reads
+        // Row units of sequence b, and the key tiles unit `pr` of it reads
         // (a malformed sequence counts 1; decode_item flags it).
+        const int unit = use_head_pairs(p.Hq, p.Hkv) ? kBM : kQTiles * kBM;
         auto seq_pairs = [&](int b, int &L, int &Lk) {
             const int qs = __ldg(p.cu_seqlens_q + b);
             L = __ldg(p.cu_seqlens_q + b + 1) - qs;
             const int ks = __ldg(p.cu_seqlens_k + b);
             Lk = __ldg(p.cu_seqlens_k + b + 1) - ks;
-            const int np = L > 0 ? (L + kQTiles * kBM - 1) / (kQTiles * kBM) : 0;
+            const int np = L > 0 ? (L + unit - 1) / unit : 0;
             return np < n_pairs ? np : n_pairs;
         };
         auto tiles_of = [&](int pr, int L, int Lk) {
             if (Lk < L || Lk <= 0) return 1;
-            const int last_row = min(L, (pr + 1) * kQTiles * kBM) - 1;
+            const int last_row = min(L, (pr + 1) * unit) - 1;
             const int t = (Lk - L + last_row) / kBN + 1;
             return t < 1 ? 1 : (t > 512 ? 512 : t);
         };
@@ -292,7 +310,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         if (tid == 0) sch->compact = compact ? 1 : 0;
         __syncthreads();
-        if (sch->compact) n_items = E * p.Hq;
+        if (sch->compact) n_items = E * (use_head_pairs(p.Hq, p.Hkv) ? p.Hq / 2 : p.Hq);
     }
 
     if (threadIdx.x == 0) {
@@ -470,9 +488,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 mbar_arrive_expect_tx(&bars->q_full, has1 ? 2 * kTileBytes : kTileBytes);
                 for (int a = 0; a < (has1 ? 2 : 1); ++a) {
                     uint8_t *sQ = smem + kOffQ + a * kTileBytes;
-                    const int row = it.q_start + it.q0 + a * kBM;
-                    tma_load_3d_hint(sQ, &q_map, &bars->q_full, 0, it.h, row, pol_first);
-                    tma_load_3d_hint(sQ + kHalf, &q_map, &bars->q_full, 64, it.h, row, pol_first);
+                    const int row = it.q_start + it.qa[a];
+                    tma_load_3d_hint(sQ, &q_map, &bars->q_full, 0, it.ha[a], row, pol_first);
+                    tma_load_3d_hint(sQ + kHalf, &q_map, &bars->q_full, 64, it.ha[a], row,
+                                     pol_first);
                 }
                 ++qcnt;
                 ok = load_k(it, 0);
@@ -649,7 +668,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             // row `row` sees key c of tile j iff c <= vis_row - 128 j.  Without
             // it (Lk == Lq) only the diagonal tile masks, at c <= row.
             const int mask_from = kOffset ? (a ? it.mask_from[1] : it.mask_from[0]) : last;
-            const int vis_row = kOffset ? it.off + it.q0 + a * kBM + row : 0;
+            const int vis_row = kOffset ? it.off + (a ? it.qa[1] : it.qa[0]) + row : 0;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; ok && j <= last; ++j) {
                 if (!mbar_wait(&bars->s_full[a], scnt & 1)) {
@@ -852,9 +871,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
             }
             ++ocnt;
             tc_fence_after();
-            const int qpos = it.q0 + a * kBM + row;
+            const int qpos = (a ? it.qa[1] : it.qa[0]) + row;
             const float inv_l = 1.f / l;
-            uint16_t *orow = p.o + ((int64_t)(it.q_start + qpos) * p.Hq + it.h) * 128;
+            uint16_t *orow =
+                p.o + ((int64_t)(it.q_start + qpos) * p.Hq + (a ? it.ha[1] : it.ha[0])) * 128;
             const bool o_aligned32 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
             uint32_t rb[2][32];
             tmem_ld32(lane_addr + col_o, rb[0]);
@@ -918,9 +938,11 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    const int n_pairs = (p.max_seqlen_q + kQTiles * kBM - 1) / (kQTiles * kBM);
+    const bool hp = use_head_pairs(p.Hq, p.Hkv);
+    const int unit = hp ? kBM : kQTiles * kBM;
+    const int n_pairs = (p.max_seqlen_q + unit - 1) / unit;     // row units per sequence
     if (p.B == 0 || n_pairs == 0) return cudaSuccess;
-    const int64_t items = (int64_t)n_pairs * p.B * p.Hq;
+    const int64_t items = (int64_t)n_pairs * p.B * (hp ? p.Hq / 2 : p.Hq);
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
