@@ -71,7 +71,10 @@ def test_prefill_exact_tiles():
     case(503, [256], 2, 1)
 
 
-@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (8, 2)])
+# Work items pair two query heads of a kv head at the same rows when the
+# group size is even (4/2, 8/2) and two adjacent row tiles of one head when it
+# is odd (2/2, 6/2); both shapes are covered.
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (6, 2), (8, 2)])
 @pytest.mark.parametrize("dynamic", [True, False])
 def test_prefill_ragged_packed_sequences(hq, hkv, dynamic):
     case(510 + hq, [1, 127, 128, 129, 300, 37, 2], hq, hkv, dynamic=dynamic)
@@ -188,7 +191,7 @@ def _paged_case(seed, prefix, new, hq, hkv, nan_tail=True, rows=None, spare=3, d
     return got, ref
 
 
-@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2), (32, 8)])
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (6, 2), (8, 2), (32, 8)])
 def test_prefill_paged_prefix_hit(hq, hkv):
     got, ref = _paged_case(540 + hq, prefix=[0, 37, 256, 300, 511, 1000],
                            new=[5, 1, 128, 200, 129, 300], hq=hq, hkv=hkv)
