@@ -696,7 +696,23 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     // Tie the maxima to the wait so no use is scheduled above it.
                     asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
                 } else {
-                    if constexpr (kOffset) {
+                    // Masked tile.  The reducing loads give the max over all 128
+                    // columns, masked ones included: an upper bound of the visible
+                    // max.  If it stays within the lazy-rescale threshold of the
+                    // running max for every row of the warp, no rescale follows
+                    // whatever the exact visible max is, so it is not computed
+                    // (the result is the same, bit for bit).  A NaN or inf in a
+                    // masked column fails the test and takes the exact path.
+                    float ub[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ub[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
+                    tmem_wait_ld();
+                    asm volatile("" : "+f"(ub[0]), "+f"(ub[1]), "+f"(ub[2]), "+f"(ub[3]));
+                    const float ub_all = fmax3(fmaxf(ub[0], ub[1]), ub[2], ub[3]);
+                    const bool exact = !__all_sync(0xffffffffu,
+                                                   ub_all * sl2 <= m_used + kRescaleThreshold);
+                    if (!exact) {
+                    } else if constexpr (kOffset) {
                         // Masked, with a key offset (masked tiles are common): the
                         // warp's rows see keys up to vis_lo .. vis_hi (lanes are
                         // consecutive rows), so each 32-column chunk is visible to every
