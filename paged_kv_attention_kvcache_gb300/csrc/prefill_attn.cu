@@ -688,10 +688,16 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 float mx4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) mx4[e] = -INFINITY;
+                // Pass 2's score chunks, two in flight.  Every path through pass 1
+                // leaves chunk 0's scores in rb[0], so pass 2 starts without a
+                // TMEM round trip of its own.
+                uint32_t rb[2][32];
                 if (!diag) {
-                    // The loads reduce: four chunk maxima, one wait.
+                    // The loads reduce: four chunk maxima, one wait; the first
+                    // keeps its scores.
+                    mx4[0] = tmem_ld32_max(lane_addr + col_s, rb[0]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) mx4[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
+                    for (int c = 1; c < 4; ++c) mx4[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
                     tmem_wait_ld();
                     // Tie the maxima to the wait so no use is scheduled above it.
                     asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
@@ -704,8 +710,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     // (the result is the same, bit for bit).  A NaN or inf in a
                     // masked column fails the test and takes the exact path.
                     float ub[4];
+                    ub[0] = tmem_ld32_max(lane_addr + col_s, rb[0]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) ub[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
+                    for (int c = 1; c < 4; ++c) ub[c] = tmem_ld32_max(lane_addr + col_s + c * 32);
                     tmem_wait_ld();
                     asm volatile("" : "+f"(ub[0]), "+f"(ub[1]), "+f"(ub[2]), "+f"(ub[3]));
                     const float ub_all = fmax3(fmaxf(ub[0], ub[1]), ub[2], ub[3]);
@@ -738,16 +745,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                                 mx4[c] = fmaxf(m2[0], m2[1]);
                             }
                         }
+                        tmem_ld32(lane_addr + col_s, rb[0]);   // chunk 0 again, for pass 2
                         tmem_wait_ld();
                         asm volatile("" : "+f"(mx4[0]), "+f"(mx4[1]), "+f"(mx4[2]), "+f"(mx4[3]));
                     } else {
-                        // Masked: the next chunk's load is in flight while this one is reduced.
-                        uint32_t rb[2][32];
-                        tmem_ld32(lane_addr + col_s, rb[0]);
-                        tmem_wait_ld();
+                        // Masked: the next chunk's load is in flight while this one is
+                        // reduced; the last step reloads chunk 0 for pass 2.
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);
+                            tmem_ld32(lane_addr + col_s + ((c + 1) & 3) * 32, rb[(c + 1) & 1]);
                             const uint32_t (&r)[32] = rb[c & 1];
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
@@ -755,7 +761,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                                 const float x1 = c * 32 + 2 * e + 1 <= vis ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
                                 mx4[e & 3] = fmax3(mx4[e & 3], x0, x1);
                             }
-                            if (c < 3) tmem_wait_ld();
+                            tmem_wait_ld();
                         }
                     }
                 }
@@ -787,9 +793,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                 float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 const float neg_m = -m_used;
                 if (!diag) {
-                    uint32_t rb[2][32];
-                    tmem_ld32(lane_addr + col_s, rb[0]);
-                    tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         // Chunk c + 1's scores (columns 32c + 32 ..) are loaded before
@@ -821,9 +824,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                                 for (int e = 0; e < 16; ++e) pk[e] = 0u;
                             } else {
-                                uint32_t r[32];
-                                tmem_ld32(lane_addr + col_s + c * 32, r);
-                                tmem_wait_ld();
+                                uint32_t rt[32];
+                                if (c > 0) {
+                                    tmem_ld32(lane_addr + col_s + c * 32, rt);
+                                    tmem_wait_ld();
+                                }
+                                const uint32_t (&r)[32] = c == 0 ? rb[0] : rt;
                                 if (c * 32 + 31 <= vis_lo) {
 #pragma unroll
                                     for (int e = 0; e < 16; ++e) {
@@ -850,9 +856,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                             tmem_st16(lane_addr + col_s + c * 16, pk);
                         }
                     } else {
-                        uint32_t rb[2][32];
-                        tmem_ld32(lane_addr + col_s, rb[0]);
-                        tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             if (c < 3) tmem_ld32(lane_addr + col_s + (c + 1) * 32, rb[(c + 1) & 1]);

@@ -74,9 +74,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // The maximum of the thread's 32 fp32 columns, reduced by the load itself
-// (tcgen05.ld.red, sm_103a).  The loaded values are not used.
-__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr) {
-    [[maybe_unused]] uint32_t r[32];
+// (tcgen05.ld.red, sm_103a); the 32 values land in r as with a plain load.
+__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32]) {
     float mx;
     asm volatile(
         "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
@@ -90,6 +89,12 @@ __device__ __forceinline__ float tmem_ld32_max(uint32_t taddr) {
           "=r"(r[31]), "=f"(mx)
         : "r"(taddr));
     return mx;
+}
+
+// As above, the loaded values not used.
+__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr) {
+    [[maybe_unused]] uint32_t r[32];
+    return tmem_ld32_max(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
