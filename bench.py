@@ -57,7 +57,7 @@ DECODE_TRAFFIC = {"ratio": 1.0036, "source_sha256_16": "ee2678ee523db987"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1165800000, "source_sha256_16": "a7e47b34f344d215"}
+PREFILL_TRAFFIC = {"bytes": 1165956352, "source_sha256_16": "c3edff9e997371cf"}
 
 
 def max_over_ranks(values, world: int, device=None):
