@@ -401,8 +401,18 @@ int decode_resolve_split(int B, int Hkv, int max_blocks, int block_size, int kv_
         // context at least four splits and the grid twelve CTAs per SM.
         // (Measured on GB300 against fixed splits: the best or within 1% on
         // B = 64 x 4k, 256 x 8k and 32 x 40k contexts; 1024-key splits lost
-        // 5% on the last.)  Otherwise, enough CTAs for several waves of two
-        // CTAs per SM, with splits no shorter than 256 keys.
+        // 5% on the last.)
+        //
+        // Otherwise (short contexts, or few sequences for their length):
+        // 1024 keys, or no split at all when the longest context is at most
+        // 2048 keys and there are at least as many (sequence, kv head) pairs
+        // as SMs; halved (to >= 512) only while the grid has fewer CTAs than
+        // half the SMs.  Here the fixed cost of a CTA (first loads, combine,
+        // partial result) and of the merge outweighs spreading the keys:
+        // sweeps over B = 8..256 with contexts up to 8192 keys, uniform and
+        // varied, found 256- and 512-key splits slower than 1024 almost
+        // everywhere (by up to 30% at B = 32..64 with 1024-key contexts),
+        // even where the longer splits leave the grid below one CTA per SM.
         split = 0;
         for (const int64_t cand : {4096, 3072, 2048, 1536}) {
             if (4 * cand <= max_ctx &&
@@ -412,9 +422,9 @@ int decode_resolve_split(int B, int Hkv, int max_blocks, int block_size, int kv_
             }
         }
         if (split == 0) {
-            split = 1024;
-            const int64_t target = 8LL * num_sms;
-            while (split > 256 && (int64_t)B * Hkv * ((max_ctx + split - 1) / split) < target)
+            const int64_t pairs = (int64_t)B * Hkv;
+            split = (max_ctx <= 2048 && pairs >= num_sms) ? 2048 : 1024;
+            while (split > 512 && 2 * pairs * ((max_ctx + split - 1) / split) < num_sms)
                 split /= 2;
         }
     }
