@@ -413,16 +413,26 @@ int decode_resolve_split(int B, int Hkv, int max_blocks, int block_size, int kv_
         // varied, found 256- and 512-key splits slower than 1024 almost
         // everywhere (by up to 30% at B = 32..64 with 1024-key contexts),
         // even where the longer splits leave the grid below one CTA per SM.
+        //
+        // A single long sequence, too short of CTAs for that, takes the
+        // longest of those splits that fills the GPU in one wave of one or
+        // two CTAs per SM (40960 keys: 2048-key splits, 26% faster than
+        // 1024).  With two or more sequences the host sees only the longest
+        // context: shorter ones leave such a grid half empty (B = 2, 4 with
+        // contexts up to 40960 keys ran 15-30% slower so), and the rule
+        // below applies.
+        const int64_t pairs = (int64_t)B * Hkv;
         split = 0;
         for (const int64_t cand : {4096, 3072, 2048, 1536}) {
+            const int64_t ctas = pairs * ((max_ctx + cand - 1) / cand);
             if (4 * cand <= max_ctx &&
-                (int64_t)B * Hkv * ((max_ctx + cand - 1) / cand) >= 12LL * num_sms) {
+                (ctas >= 12LL * num_sms ||
+                 (B == 1 && ctas >= num_sms && ctas <= 2LL * num_sms))) {
                 split = cand;
                 break;
             }
         }
         if (split == 0) {
-            const int64_t pairs = (int64_t)B * Hkv;
             split = (max_ctx <= 2048 && pairs >= num_sms) ? 2048 : 1024;
             while (split > 512 && 2 * pairs * ((max_ctx + split - 1) / split) < num_sms)
                 split /= 2;
