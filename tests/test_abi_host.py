@@ -139,6 +139,33 @@ def test_decode_rejects_bad_arguments_and_small_workspace(lib):
     assert call(B=0) == NV_OK
 
 
+def test_decode_automatic_split_choices(lib):
+    """The automatic split (kv_split_tokens = 0), read back through the
+    workspace query: B * Hq * splits * (128 + 1) floats.  Without a GPU the
+    library assumes GB300's 152 SMs."""
+    def splits(B, Hq, Hkv, ctx):
+        ws = lib.nv_decode_attn_workspace_size(B, Hq, Hkv, 128, ctx // 256, 256, 0)
+        assert ws % (B * Hq * 129 * 4) == 0
+        return max(1, ws // (B * Hq * 129 * 4))
+
+    # The configured decode sets: 1024-, 2048- and 4096-key splits.
+    assert splits(64, 16, 8, 4096) == 4
+    assert splits(256, 32, 8, 8192) == 4
+    assert splits(32, 32, 8, 40960) == 10
+    # Short contexts over at least one (sequence, kv head) pair per SM: unsplit.
+    assert splits(64, 32, 8, 1024) == 1
+    assert splits(32, 32, 8, 2048) == 1
+    # Fewer pairs: 1024-key splits, halved only while the grid has fewer CTAs
+    # than half the SMs, and never below 512 keys.
+    assert splits(16, 32, 8, 2048) == 2
+    assert splits(8, 32, 8, 1024) == 2
+    assert splits(8, 32, 8, 512) == 1
+    assert splits(1, 32, 8, 8192) == 16
+    # A single long sequence fills one wave (2048-key splits); two do not.
+    assert splits(1, 32, 8, 40960) == 20
+    assert splits(2, 32, 8, 40960) == 40
+
+
 def test_rope_table_rejects_bad_arguments(lib):
     f = lib.nv_rope_cos_sin_cache
     assert f(FAKE, 16, 127, 1e6, None) == NV_EINVAL
