@@ -345,7 +345,11 @@ NV_API size_t nv_decode_attn_workspace_size(int B, int Hq, int Hkv, int head_dim
  *   context_lens  [B] int32.
  *   o             [B, Hq, head_dim] bf16, contiguous, written.
  *   kv_split_tokens  keys per split (rounded up to a multiple of 64);
- *                 0 = automatic.  A sequence longer than one split is
+ *                 0 = automatic: chosen from B, Hkv, the longest context
+ *                 (max_blocks_per_seq * block_size) and the SM count,
+ *                 usually 1024-4096 keys, 512 for a very small grid; short
+ *                 contexts over many sequences are not split at all.  A
+ *                 sequence longer than one split is
  *                 processed by several CTAs whose partial (O, log-sum-exp)
  *                 go to `workspace` and are merged by a second kernel.
  *   workspace     device buffer of at least
