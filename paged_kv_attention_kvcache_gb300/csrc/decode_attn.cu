@@ -451,17 +451,12 @@ size_t decode_workspace_bytes(int B, int Hq, int max_splits) {
 
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, cudaStream_t s) {
-    static bool attr_done = false;   // benign race: setting it twice is harmless
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kDecodeSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = ensure_dynamic_smem(decode_split_kernel, kDecodeSmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
     if (p.B == 0) return cudaSuccess;
     dim3 grid(p.max_splits, p.Hkv, p.B);
-    cudaError_t e = launch_pdl(decode_split_kernel, grid, dim3(kDecodeThreads),
+    e = launch_pdl(decode_split_kernel, grid, dim3(kDecodeThreads),
                                (size_t)kDecodeSmemBytes, s, k_map, v_map, p);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     const int64_t warps = (int64_t)p.B * p.Hq;

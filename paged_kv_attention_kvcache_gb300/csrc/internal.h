@@ -9,6 +9,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace nvattn {
 
 // Blocks of `kernel` (with `threads` threads and no dynamic shared memory)
@@ -23,6 +25,22 @@ inline int64_t resident_grid(void (*kernel)(KArgs...), int threads, int fallback
             cudaSuccess || sms <= 0 || per_sm <= 0)
         return (int64_t)152 * fallback_per_sm;
     return (int64_t)sms * per_sm;
+}
+
+// Allows `kernel` `bytes` of dynamic shared memory on the current device.
+// The attribute belongs to each device's context, so it is set once per
+// device (bit d of `done` for device d < 64; always for higher ordinals).
+template <typename... KArgs>
+inline cudaError_t ensure_dynamic_smem(void (*kernel)(KArgs...), int bytes,
+                                       std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
 }
 
 // Launch with programmatic stream serialization (see pdl_wait_release).

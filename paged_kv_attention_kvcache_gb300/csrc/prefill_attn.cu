@@ -949,14 +949,10 @@ template <bool kPaged, bool kOffset>
 static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q_map,
                                     const CUtensorMap &k_map, const CUtensorMap &v_map,
                                     cudaStream_t s) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<kPaged, kOffset>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kPrefillSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    const cudaError_t ea = ensure_dynamic_smem(prefill_attn_kernel<kPaged, kOffset>,
+                                               kPrefillSmemBytes, smem_set);
+    if (ea != cudaSuccess) return ea;
     const bool hp = use_head_pairs(p.Hq, p.Hkv);
     const int unit = hp ? kBM : kQTiles * kBM;
     const int n_pairs = (p.max_seqlen_q + unit - 1) / unit;     // row units per sequence
@@ -965,7 +961,7 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        sms = 148;
+        sms = 152;
     // Persistent: one CTA per SM.  The work counter starts every launch at 0.
     const int grid = (int)(items < sms ? items : sms);
     if (p.work_counter) {
