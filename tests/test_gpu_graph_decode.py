@@ -43,9 +43,13 @@ def _step_inputs(seed, bucket, n_real, ctx, bt, pos_shift=0):
     return dict(qkv=qkv, x=x, r=r, ctx=c, pos=pos, slots=slots)
 
 
-@pytest.mark.parametrize("bucket,n_real,fused", [(1, 1, False), (8, 5, False), (64, 61, False),
-                                                 (8, 5, True), (512, 509, True)])
-def test_decode_layer_graph_replay_with_padding(bucket, n_real, fused):
+# Forced 256-key splits exercise the split + merge pair inside the graph; the
+# automatic split leaves these short contexts unsplit at buckets 64 and 512
+# (one decode kernel) and takes 1024-key splits at bucket 8.
+@pytest.mark.parametrize("bucket,n_real,fused,split", [
+    (1, 1, False, 256), (8, 5, False, 256), (64, 61, False, 256), (8, 5, True, 256),
+    (512, 509, True, 256), (8, 5, False, 0), (64, 61, False, 0), (512, 509, True, 0)])
+def test_decode_layer_graph_replay_with_padding(bucket, n_real, fused, split):
     s = SHAPE
     Q, D = s.q_size, s.kv_size
     g = np.random.default_rng(700 + bucket)
@@ -74,8 +78,9 @@ def test_decode_layer_graph_replay_with_padding(bucket, n_real, fused):
     d_bt = torch.from_numpy(bt).cuda()
     o = torch.zeros(bucket, s.hq, 128, dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    split = 256
     ws_b = nv.nv_decode_attn_workspace_size(bucket, s.hq, s.hkv, 128, bt.shape[1], 256, split)
+    if split == 0:                                  # what the automatic split chose here
+        assert (ws_b > 0) == (bucket == 8)
     ws = torch.empty(max(1, ws_b // 4), dtype=torch.float32, device="cuda")
     q = qkv[:, :Q].view(bucket, s.hq, 128)
     k = qkv[:, Q:Q + D].view(bucket, s.hkv, 128)
