@@ -411,8 +411,9 @@ int decode_resolve_split(int B, int Hkv, int max_blocks, int block_size, int kv_
         // partial result) and of the merge outweighs spreading the keys:
         // sweeps over B = 8..256 with contexts up to 8192 keys, uniform and
         // varied, found 256- and 512-key splits slower than 1024 almost
-        // everywhere (by up to 30% at B = 32..64 with 1024-key contexts),
-        // even where the longer splits leave the grid below one CTA per SM.
+        // everywhere (by up to 30%, at B = 16..64 with contexts of 512 to
+        // 2048 keys), even where the longer splits leave the grid below one
+        // CTA per SM.
         //
         // A single long sequence, too short of CTAs for that, takes the
         // longest of those splits that fills the GPU in one wave of one or
