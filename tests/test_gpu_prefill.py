@@ -72,12 +72,13 @@ def test_prefill_exact_tiles():
 
 
 # Work items pair two query heads of a kv head at the same rows when the
-# group size is even (4/2, 8/2) and two adjacent row tiles of one head when it
-# is odd (2/2, 6/2); both shapes are covered.
-@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (6, 2), (8, 2)])
+# group size is even (4/2, 8/2, 8/1, 16/1) and two adjacent row tiles of one
+# head when it is odd (2/2, 6/2, 5/1); both shapes are covered, up to the
+# group of 16 the decode supports.
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (6, 2), (8, 2), (8, 1), (16, 1), (5, 1)])
 @pytest.mark.parametrize("dynamic", [True, False])
 def test_prefill_ragged_packed_sequences(hq, hkv, dynamic):
-    case(510 + hq, [1, 127, 128, 129, 300, 37, 2], hq, hkv, dynamic=dynamic)
+    case(510 + hq + 100 * (hkv == 1), [1, 127, 128, 129, 300, 37, 2], hq, hkv, dynamic=dynamic)
 
 
 def test_prefill_more_items_than_ctas_both_schedules_agree():
