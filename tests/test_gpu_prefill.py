@@ -81,6 +81,17 @@ def test_prefill_ragged_packed_sequences(hq, hkv, dynamic):
     case(510 + hq + 100 * (hkv == 1), [1, 127, 128, 129, 300, 37, 2], hq, hkv, dynamic=dynamic)
 
 
+def test_prefill_sequences_without_query_rows():
+    # A sequence with no new rows (cu_seqlens repeating a value, as when a
+    # sequence adds nothing in this step) brings no work item; its neighbours
+    # must still match the oracle, under both schedules and over the paged
+    # cache (where such a sequence may still own cached keys).
+    for dynamic in (True, False):
+        case(560, [0, 37, 0, 0, 300, 0, 129], 8, 2, dynamic=dynamic)
+    got, ref = _paged_case(561, prefix=[300, 0, 512, 40], new=[0, 37, 0, 129], hq=8, hkv=2)
+    check_close(got, ref, "paged prefill next to sequences without new rows")
+
+
 def test_prefill_more_items_than_ctas_both_schedules_agree():
     # 40 sequences x 8 heads of up to 1000 tokens: several items per CTA under
     # either schedule; both must give the oracle's result on every row.
