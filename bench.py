@@ -1214,9 +1214,11 @@ def main():
     __graft_entry__.build()
     r = run_ours(args, rank, world, local_rank)
 
+    # The oracle is timed on the host cores beside a single-GPU run only; with
+    # several replicas the line reports the GPUs alone.
     cpu = None
     ofig = {}
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         val, threads, reps, secs = oracle_baseline(r["step"])
         cpu = {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "tokens_per_s": r["step"].context_lens.size * reps / secs,
