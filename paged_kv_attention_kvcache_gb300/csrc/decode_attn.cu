@@ -457,8 +457,16 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &k_map,
     if (e != cudaSuccess) return e;
     if (p.B == 0) return cudaSuccess;
     dim3 grid(p.max_splits, p.Hkv, p.B);
-    e = launch_pdl(decode_split_kernel, grid, dim3(kDecodeThreads),
-                               (size_t)kDecodeSmemBytes, s, k_map, v_map, p);
+    e = launch_pdl(decode_split_kernel, grid, dim3(kDecodeThreads), (size_t)kDecodeSmemBytes, s,
+                   k_map, v_map, p);
+    if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) {
+        // The shared-memory attribute was lost (the device was reset): set it again, retry once.
+        cudaGetLastError();
+        e = ensure_dynamic_smem(decode_split_kernel, kDecodeSmemBytes, smem_set, true);
+        if (e == cudaSuccess)
+            e = launch_pdl(decode_split_kernel, grid, dim3(kDecodeThreads),
+                           (size_t)kDecodeSmemBytes, s, k_map, v_map, p);
+    }
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     const int64_t warps = (int64_t)p.B * p.Hq;
     return launch_pdl(decode_merge_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256),

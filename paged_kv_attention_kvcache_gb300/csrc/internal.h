@@ -29,15 +29,16 @@ inline int64_t resident_grid(void (*kernel)(KArgs...), int threads, int fallback
 
 // Allows `kernel` `bytes` of dynamic shared memory on the current device.
 // The attribute belongs to each device's context, so it is set once per
-// device (bit d of `done` for device d < 64; always for higher ordinals).
+// device (bit d of `done` for device d < 64; always for higher ordinals);
+// `force` sets it again (a launch found it missing: the device was reset).
 template <typename... KArgs>
 inline cudaError_t ensure_dynamic_smem(void (*kernel)(KArgs...), int bytes,
-                                       std::atomic<uint64_t> &done) {
+                                       std::atomic<uint64_t> &done, bool force = false) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
-    if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    if (!force && bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
     return e;

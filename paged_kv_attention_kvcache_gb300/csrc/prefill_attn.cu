@@ -968,8 +968,20 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &q
         const cudaError_t e = cudaMemsetAsync(p.work_counter, 0, sizeof(int), s);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(prefill_attn_kernel<kPaged, kOffset>, dim3(grid), dim3(kPrefillThreads),
-                      (size_t)kPrefillSmemBytes, s, q_map, k_map, v_map, p, n_pairs, (int)items);
+    cudaError_t e = launch_pdl(prefill_attn_kernel<kPaged, kOffset>, dim3(grid),
+                               dim3(kPrefillThreads), (size_t)kPrefillSmemBytes, s, q_map, k_map,
+                               v_map, p, n_pairs, (int)items);
+    if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) {
+        // The shared-memory attribute was lost (the device was reset): set it again, retry once.
+        cudaGetLastError();
+        e = ensure_dynamic_smem(prefill_attn_kernel<kPaged, kOffset>, kPrefillSmemBytes,
+                                smem_set, true);
+        if (e == cudaSuccess)
+            e = launch_pdl(prefill_attn_kernel<kPaged, kOffset>, dim3(grid),
+                           dim3(kPrefillThreads), (size_t)kPrefillSmemBytes, s, q_map, k_map,
+                           v_map, p, n_pairs, (int)items);
+    }
+    return e;
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &q_map,
