@@ -53,11 +53,11 @@ SCALE = 128 ** -0.5
 # decode_split_kernel and decode_merge_kernel over the algorithmic bytes),
 # valid only for the kernel code it was taken on (the hash ignores comments
 # and layout).
-DECODE_TRAFFIC = {"ratio": 1.0035, "source_sha256_16": "f8216c4ccfa696af"}
+DECODE_TRAFFIC = {"ratio": 1.0036, "source_sha256_16": "5574a127e6991e65"}
 # DRAM bytes (read + write) of one prefill-attention launch on the bench batch
 # (33,109 tokens, Qwen3-8B heads): mean of the two launches of an ncu capture
 # of `bench.py --ncu-case layer` (cold L2, as ncu runs each launch).
-PREFILL_TRAFFIC = {"bytes": 1179374720, "source_sha256_16": "5e70c197b7dd8881"}
+PREFILL_TRAFFIC = {"bytes": 1179100800, "source_sha256_16": "2e2f80d5fe096d24"}
 
 
 def max_over_ranks(values, world: int, device=None):
